@@ -1,0 +1,35 @@
+"""CPU oracle for one TwoTower denoise step: plain numpy, fp64 arithmetic.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product imports this package: only the
+tests, ``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import, call or execute anything under ``oracle/``.  It shares no
+code with the CUDA path; its inputs come from the seeded generators in
+``block_wise_mask_tt_b300.synth`` (which hold none of the method's arithmetic) or
+from the tests themselves.
+
+Sources ("Nemotron-Labs-TwoTower" wiki page unless stated otherwise):
+* adaLN time conditioning - sections "Motivation: one network, two roles" and
+  "Ablations" (adaptive layer normalization on the diffusion timestep);
+* denoise attention - section "Architecture" (block queries attend over the context
+  tower's layer-i cache followed by the block's own keys, bidirectional in the block);
+* confidence unmasking and the timestep rule - section "Block-wise generation".
+
+Every function computes the plain definition: no blocking, no fusion, no reordering
+beyond what the definition states.  Readings where the pages are silent are listed
+in each module's docstring.
+"""
+from .adaln import adaln_modulate
+from .attention import denoise_attention, denoise_attention_rows, context_kv
+from .unmask import row_confidence, unmask_step
+from .loop import denoise_block, denoise_block_batch
+
+__all__ = [
+    "adaln_modulate",
+    "denoise_attention",
+    "denoise_attention_rows",
+    "context_kv",
+    "row_confidence",
+    "unmask_step",
+    "denoise_block",
+    "denoise_block_batch",
+]

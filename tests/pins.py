@@ -1,0 +1,337 @@
+"""Checks that pin the oracle to something other than itself.
+
+Each ``check_*`` takes the oracle function(s) under test as arguments, so that the
+same checks run against the real oracle (tests/test_oracle_*.py) and against copies
+with a planted mistake (tests/test_oracle_mutations.py), which they must reject.
+The pins are library routines other than the ones the oracle calls (torch SDPA and
+layer_norm, scipy softmax), closed forms, invariants and special cases.
+"""
+import math
+
+import numpy as np
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+from block_wise_mask_tt_b300 import synth
+
+
+# ----------------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------------
+
+def tiny_attention_inputs(seed, B, S, Hq, Hkv, D, lens, paged=False, page_size=4):
+    w = synth.Workload("tiny", B=B, L=max(lens) if len(lens) else 0, S=S, Hq=Hq, Hkv=Hkv, D=D,
+                       H=8, V=16, paged=paged, page_size=page_size,
+                       L_min=1 if paged else 0)
+    return synth.make_attention_inputs(w, seed, ctx_len=np.asarray(lens, np.int32))
+
+
+def _bf(x):
+    return torch.from_numpy(synth.bf16_bits_to_f32(x).astype(np.float64))
+
+
+def torch_reference(inp, scale):
+    """torch SDPA (fp64, CPU) over [context ++ block] keys per sequence; lse by logsumexp."""
+    q = _bf(inp["q"])  # B S Hq D
+    kb, vb = _bf(inp["k_blk"]), _bf(inp["v_blk"])
+    B, S, Hq, D = q.shape
+    Hkv = kb.shape[2]
+    G = Hq // Hkv
+    outs, lses = [], []
+    for b in range(B):
+        n = int(inp["ctx_len"][b])
+        if "page_table" in inp:
+            ps = inp["k_pages"].shape[1]
+            kc = torch.stack([_bf(inp["k_pages"][inp["page_table"][b, t // ps], t % ps])
+                              for t in range(n)]) if n else torch.zeros(0, Hkv, D, dtype=torch.float64)
+            vc = torch.stack([_bf(inp["v_pages"][inp["page_table"][b, t // ps], t % ps])
+                              for t in range(n)]) if n else torch.zeros(0, Hkv, D, dtype=torch.float64)
+        else:
+            kc, vc = _bf(inp["k_ctx"][b, :n]), _bf(inp["v_ctx"][b, :n])
+        k = torch.cat([kc, kb[b]], 0).permute(1, 0, 2).repeat_interleave(G, 0)  # Hq, L+S, D
+        v = torch.cat([vc, vb[b]], 0).permute(1, 0, 2).repeat_interleave(G, 0)
+        qq = q[b].permute(1, 0, 2)  # Hq S D
+        o = F.scaled_dot_product_attention(qq[None], k[None], v[None], scale=scale)[0]
+        outs.append(o.permute(1, 0, 2))
+        lses.append(torch.logsumexp(scale * qq @ k.transpose(1, 2), dim=-1).permute(1, 0))
+    return torch.stack(outs).numpy(), torch.stack(lses).numpy()
+
+
+def check_attention_vs_torch(attn_fn):
+    cases = [
+        dict(B=2, S=3, Hq=4, Hkv=2, D=8, lens=[5, 0]),
+        dict(B=1, S=16, Hq=4, Hkv=1, D=16, lens=[37]),
+        dict(B=3, S=1, Hq=6, Hkv=3, D=8, lens=[1, 9, 4]),
+        dict(B=2, S=5, Hq=2, Hkv=2, D=4, lens=[13, 2]),
+    ]
+    for i, c in enumerate(cases):
+        for paged in (False, True):
+            inp = tiny_attention_inputs(100 + i, paged=paged, **c)
+            scale = 1.0 / math.sqrt(c["D"])
+            O, lse = attn_fn(inp, scale)
+            Ot, lset = torch_reference(inp, scale)
+            np.testing.assert_allclose(O, Ot, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(lse, lset, rtol=1e-12, atol=1e-12)
+
+
+def check_identical_keys_mean(attn_fn):
+    """Every key equal => uniform weights => output is the mean of all value rows."""
+    B, S, Hq, Hkv, D, L = 2, 4, 4, 2, 8, 6
+    inp = tiny_attention_inputs(7, B, S, Hq, Hkv, D, [L, L])
+    key = synth.f32_to_bf16_bits(np.linspace(-1, 1, D).astype(np.float32))
+    inp["k_ctx"][:] = key
+    inp["k_blk"][:] = key
+    O, _ = attn_fn(inp, 0.7)
+    vc = synth.bf16_bits_to_f32(inp["v_ctx"]).astype(np.float64)
+    vb = synth.bf16_bits_to_f32(inp["v_blk"]).astype(np.float64)
+    G = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            mean = np.concatenate([vc[b, :L, g], vb[b, :, g]]).mean(axis=0)
+            for s in range(S):
+                np.testing.assert_allclose(O[b, s, h], mean, rtol=1e-12, atol=1e-12)
+
+
+def check_block_permutation(attn_fn):
+    """Bidirectional block: permuting block tokens (q, k_blk, v_blk together) permutes O."""
+    inp = tiny_attention_inputs(8, 2, 6, 4, 2, 8, [5, 3])
+    O, lse = attn_fn(inp, 0.35)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    inp2 = dict(inp)
+    for k in ("q", "k_blk", "v_blk"):
+        inp2[k] = inp[k][:, perm]
+    O2, lse2 = attn_fn(inp2, 0.35)
+    np.testing.assert_allclose(O2, O[:, perm], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse[:, perm], rtol=1e-12, atol=1e-12)
+
+
+def check_single_key(attn_fn):
+    """No context and a one-token block: the only key gets weight 1, O = v, lse = scale*q.k."""
+    inp = tiny_attention_inputs(9, 1, 1, 2, 1, 8, [0])
+    O, lse = attn_fn(inp, 0.5)
+    v = synth.bf16_bits_to_f32(inp["v_blk"][0, 0, 0]).astype(np.float64)
+    q = synth.bf16_bits_to_f32(inp["q"][0, 0]).astype(np.float64)
+    k = synth.bf16_bits_to_f32(inp["k_blk"][0, 0, 0]).astype(np.float64)
+    for h in range(2):
+        np.testing.assert_allclose(O[0, 0, h], v, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[0, 0, h], 0.5 * q[h] @ k, rtol=1e-12, atol=1e-12)
+
+
+def check_dominant_key(attn_fn):
+    """One context key aligned with q and much larger than the rest selects its value row."""
+    B, S, Hq, Hkv, D, L = 1, 2, 2, 1, 8, 7
+    inp = tiny_attention_inputs(10, B, S, Hq, Hkv, D, [L])
+    q = np.zeros((B, S, Hq, D), np.float32)
+    q[..., 0] = 1.0
+    inp["q"] = synth.f32_to_bf16_bits(q)
+    k = synth.bf16_bits_to_f32(inp["k_ctx"]).copy()
+    k[..., 0] = 0.0
+    k[0, 4, 0, 0] = 64.0  # exp(64*1) dominates every other weight (others are exp(0))
+    inp["k_ctx"] = synth.f32_to_bf16_bits(k)
+    kb = synth.bf16_bits_to_f32(inp["k_blk"]).copy()
+    kb[..., 0] = 0.0
+    inp["k_blk"] = synth.f32_to_bf16_bits(kb)
+    O, _ = attn_fn(inp, 1.0)
+    v = synth.bf16_bits_to_f32(inp["v_ctx"][0, 4, 0]).astype(np.float64)
+    for s in range(S):
+        for h in range(Hq):
+            np.testing.assert_allclose(O[0, s, h], v, rtol=1e-12, atol=1e-12)
+
+
+ATTENTION_CHECKS = (check_attention_vs_torch, check_identical_keys_mean, check_block_permutation,
+                    check_single_key, check_dominant_key)
+
+
+# ----------------------------------------------------------------------------------
+# adaLN
+# ----------------------------------------------------------------------------------
+
+def check_adaln_vs_torch(adaln_fn):
+    rng = np.random.default_rng(3)
+    for H in (1, 7, 256, 2688):
+        x = synth.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32) * 2 + 0.5)
+        shift = rng.standard_normal((3, H)).astype(np.float32) * 0.1
+        scale = rng.standard_normal((3, H)).astype(np.float32) * 0.1
+        y = adaln_fn(x, shift, scale, 1e-5)
+        xt = _bf(x)
+        for r in range(3):
+            ref = F.layer_norm(xt[r], (H,), weight=1 + torch.from_numpy(scale[r]).double(),
+                               bias=torch.from_numpy(shift[r]).double(), eps=1e-5).numpy()
+            np.testing.assert_allclose(y[r], ref, rtol=1e-12, atol=1e-12)
+        y0 = adaln_fn(x, np.zeros(H, np.float32), np.zeros(H, np.float32), 1e-3)
+        ref0 = F.layer_norm(xt, (H,), eps=1e-3).numpy()
+        np.testing.assert_allclose(y0, ref0, rtol=1e-12, atol=1e-12)
+
+
+def check_adaln_constant_row(adaln_fn):
+    """x constant => x - mean = 0 => y = shift exactly, whatever scale is."""
+    H = 64
+    x = np.full((2, H), synth.f32_to_bf16_bits(np.float32(1.75)), np.uint16)
+    shift = np.linspace(-1, 1, H).astype(np.float32)
+    scale = np.linspace(2, -3, H).astype(np.float32)
+    y = adaln_fn(x, shift, scale, 1e-5)
+    np.testing.assert_array_equal(y, np.broadcast_to(shift.astype(np.float64), (2, H)))
+
+
+def check_adaln_moments(adaln_fn):
+    """With shift = scale = 0 the row has mean 0 and biased variance var/(var+eps)."""
+    rng = np.random.default_rng(4)
+    H, eps = 512, 0.25
+    xf = rng.standard_normal(H).astype(np.float32)
+    x = synth.f32_to_bf16_bits(xf)
+    y = adaln_fn(x, np.zeros(H, np.float32), np.zeros(H, np.float32), eps)
+    xd = synth.bf16_bits_to_f32(x).astype(np.float64)
+    var = np.var(xd)
+    assert abs(y.mean()) < 1e-12
+    np.testing.assert_allclose(np.mean(y ** 2), var / (var + eps), rtol=1e-12)
+
+
+ADALN_CHECKS = (check_adaln_vs_torch, check_adaln_constant_row, check_adaln_moments)
+
+
+# ----------------------------------------------------------------------------------
+# unmask
+# ----------------------------------------------------------------------------------
+
+def check_conf_two_valued(row_conf_fn):
+    """Logit a at one id, b elsewhere (mask id included at b): conf = e^a/(e^a+(V-2)e^b)."""
+    for V, a, bval, j, mask in ((16, 3.0, 1.0, 9, 3), (1024, 0.5, -2.0, 0, 3), (50, 10.0, 9.0, 49, 0)):
+        row = np.full(V, bval, np.float32)
+        row[j] = a
+        tok, conf = row_conf_fn(row, mask)
+        exp = math.exp(a) / (math.exp(a) + (V - 2) * math.exp(bval))
+        assert tok == j
+        assert abs(conf - exp) <= 1e-14 * exp
+
+
+def check_conf_vs_scipy(row_conf_fn):
+    rng = np.random.default_rng(5)
+    for V in (8, 1000, 131072):
+        for mask in (3, 0, V - 1):
+            row = (rng.standard_normal(V) * 3).astype(np.float32)
+            tok, conf = row_conf_fn(row, mask)
+            keep = np.delete(np.arange(V), mask)
+            p = scipy.special.softmax(row[keep].astype(np.float64))
+            assert tok == keep[int(np.argmax(p))]
+            assert abs(conf - p.max()) <= 1e-12 * p.max()
+
+
+def check_mask_never_emitted(row_conf_fn):
+    """The mask id holds the largest logit by far: it is neither emitted nor counted."""
+    V, mask = 64, 3
+    row = np.linspace(-1, 1, V).astype(np.float32)
+    row[mask] = 50.0
+    tok, conf = row_conf_fn(row, mask)
+    assert tok == V - 1
+    keep = np.delete(row.astype(np.float64), mask)
+    assert abs(conf - 1.0 / np.sum(np.exp(keep - keep.max()))) < 1e-14
+
+
+def check_ties_lowest_id(row_conf_fn):
+    V, mask = 32, 3
+    row = np.zeros(V, np.float32)
+    for ids in ((5, 6), (30, 7, 19), (0, 31), (2, 4)):
+        r = row.copy()
+        r[list(ids)] = 2.5
+        tok, conf = row_conf_fn(r, mask)
+        assert tok == min(ids)
+        assert abs(conf - math.exp(2.5) / (len(ids) * math.exp(2.5) + (V - 1 - len(ids)))) < 1e-14
+
+
+def check_threshold_inclusive(step_fn):
+    """Two equal live logits => conf = 1/2 exactly; gamma = 0.5 commits it (>=)."""
+    V, mask, S = 3, 2, 2
+    logits = np.zeros((S, V), np.float32)
+    logits[:, mask] = 5.0
+    r = step_fn(logits, np.full(S, mask), 0, mask, 0.5, 8)
+    assert r["conf"][0] == 0.5 and r["conf"][1] == 0.5
+    assert r["commit"].tolist() == [1, 1]
+    assert r["ids"].tolist() == [0, 0]  # tie between ids 0 and 1 -> 0
+
+
+def _random_logits_fn(seed, V, mask, boost=(0.0, 12.0)):
+    def fn(step, positions):
+        return synth.logits_rows(seed, 0, 0, step, positions, V, mask, synth.LOGITS_UNIFORM, *boost)
+    return fn
+
+
+def check_gamma_zero_one_step(block_fn):
+    for seed in range(3):
+        r = block_fn(16, 16, 3, 0.0, _random_logits_fn(seed, 256, 3))
+        assert r["steps"] == 1
+        assert np.all(r["ids"] != 3)
+        assert np.all(r["commit_step"] == 1)
+
+
+def check_gamma_above_one_takes_s_steps(block_fn):
+    """gamma > 1 => only the floor commits: exactly one per step, most confident first."""
+    for S in (1, 5, 16):
+        r = block_fn(S, S, 3, 1.01, _random_logits_fn(11 + S, 256, 3))
+        assert r["steps"] == S
+        assert sorted(r["commit_step"].tolist()) == list(range(1, S + 1))
+        for tr in r["trace"]:
+            assert len(tr["committed"]) == 1
+            i = tr["committed"][0]
+            live = [p for p in range(S) if tr["ids_before"][p] == 3]
+            assert all(tr["conf"][i] > tr["conf"][p] or (tr["conf"][i] == tr["conf"][p] and i <= p)
+                       for p in live)
+
+
+def check_floor_ceil_rule(block_fn):
+    """T < S with gamma > 1: each step commits ceil(m / steps_left) positions."""
+    for S, T in ((16, 4), (16, 5), (7, 3), (32, 16)):
+        r = block_fn(S, T, 3, 2.0, _random_logits_fn(S * T, 128, 3))
+        assert r["steps"] == T
+        m = S
+        for k, tr in enumerate(r["trace"]):
+            want = math.ceil(m / (T - k))
+            assert len(tr["committed"]) == want
+            m -= want
+        assert m == 0
+
+
+def check_frozen_and_bounded(block_fn):
+    """Committed ids never change, the mask id is never emitted, steps <= T, t = m/S."""
+    for seed, gamma in ((1, 0.8), (2, 0.5), (3, 0.95), (4, 0.3)):
+        S, T = 16, 16
+        r = block_fn(S, T, 3, gamma, _random_logits_fn(seed, 512, 3, (0.0, 14.0)))
+        assert 1 <= r["steps"] <= T
+        assert np.all(r["ids"] != 3)
+        prev = None
+        for tr in r["trace"]:
+            ids_b = tr["ids_before"]
+            assert tr["t"] == np.sum(ids_b == 3) / S
+            if prev is not None:
+                done = prev != 3
+                assert np.array_equal(ids_b[done], prev[done])
+            prev = ids_b
+        assert r["trace"][0]["t"] == 1.0
+        # a position's final id is the token predicted at its commit step
+        for tr in r["trace"]:
+            for i in tr["committed"]:
+                assert r["ids"][i] == tr["tok"][i]
+        # commits above gamma are exactly the positions at or above gamma (when any exist)
+        for tr in r["trace"]:
+            live = np.flatnonzero(tr["ids_before"] == 3)
+            above = [i for i in live if tr["conf"][i] >= gamma]
+            if len(above) >= tr["k_min"]:
+                assert sorted(above) == sorted(tr["committed"].tolist())
+
+
+def check_floor_ties_lower_position(block_fn):
+    """Equal confidence everywhere and gamma > 1: the floor commits positions in order."""
+    S = 6
+
+    def fn(step, positions):
+        return np.zeros((len(positions), 16), np.float32)
+    r = block_fn(S, S, 3, 1.5, fn)
+    assert [int(tr["committed"][0]) for tr in r["trace"]] == list(range(S))
+
+
+UNMASK_ROW_CHECKS = (check_conf_two_valued, check_conf_vs_scipy, check_mask_never_emitted,
+                     check_ties_lowest_id)
+UNMASK_STEP_CHECKS = (check_threshold_inclusive,)
+BLOCK_CHECKS = (check_gamma_zero_one_step, check_gamma_above_one_takes_s_steps,
+                check_floor_ceil_rule, check_frozen_and_bounded, check_floor_ties_lower_position)
