@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Denoise steps/s of one TwoTower denoiser step on B300, plus per-kernel roofline.
+
+One bench step = one denoise step over the whole batch: adaLN(t) prologue, split-KV
+attention (context cache + the block's own keys), the synthetic-logits stand-in for
+the LM head, and confidence unmasking, all in libtt's CUDA kernels.  Blocks start
+fully masked and are decoded with tt_denoise_block_loop (a CUDA graph whose WHILE
+node repeats the step on the device until the block is committed); the step counts
+per block are deterministic (seeded logits), so an untimed pass first learns them
+and the timed region covers exactly --steps denoise steps (whole blocks, then single
+tt_denoise_step calls for the remainder).  L2 is flushed before every timed block,
+outside the timed events.
+
+Default workload: single sequence, B=1, L=4096 context, S=16, 32q/2kv heads, D=128,
+H=2688, V=131072, gamma=0.8 (--config 1).  --config 0..4 selects the other workloads.
+
+    python bench.py [--gpus N --steps K --warmup W] [--config C] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_wise_mask_tt_b300 import synth  # noqa: E402
+
+METRIC = "denoise steps/s; attention and unmask achieved % of HBM/tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100, help="timed denoise steps")
+    ap.add_argument("--warmup", type=int, default=3, help="untimed warm-up denoise steps (>= 3)")
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=("tt", "reference"), default="tt")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--gamma", type=float, default=None)
+    ap.add_argument("--kernel-reps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.5,
+                    help="keep warming up for at least this long so the clock sampler sees load")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload(args) -> synth.Workload:
+    w = synth.CONFIGS[args.config]
+    if args.gamma is not None:
+        w = w.replace(gamma=args.gamma)
+    return w
+
+
+def cores_used() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks sampler
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.dev = device_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU workload
+class Workbench:
+    """Device-resident inputs, state and buffers for one replica of the workload."""
+
+    def __init__(self, tt, torch, w: synth.Workload, seed: int):
+        self.tt, self.torch, self.w, self.seed = tt, torch, w, seed
+        t0 = time.time()
+        self.inp = synth.make_attention_inputs(w, seed)
+        self.ad = synth.make_adaln_inputs(w, seed)
+        self.gen_s = time.time() - t0
+        B, S = w.B, w.S
+        dev = lambda a: self._dev(a)
+        if w.paged:
+            kp = self.inp["k_pages"]
+            self.dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, 0, w.page_size,
+                                     self.inp["page_table"].shape[1], kp.shape[0], w.softmax_scale, 0)
+            kc, vc, pt = dev(kp), dev(self.inp["v_pages"]), dev(self.inp["page_table"])
+        else:
+            self.dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, self.inp["k_ctx"].shape[1], 0, 0, 0,
+                                     w.softmax_scale, 0)
+            kc, vc, pt = dev(self.inp["k_ctx"]), dev(self.inp["v_ctx"]), None
+        T = torch
+        self.t = dict(
+            x=dev(self.ad["x"]), shift_table=dev(self.ad["shift_table"]),
+            scale_table=dev(self.ad["scale_table"]), q=dev(self.inp["q"]),
+            k_blk=dev(self.inp["k_blk"]), v_blk=dev(self.inp["v_blk"]), k_ctx=kc, v_ctx=vc,
+            page_table=pt, ctx_len=dev(self.inp["ctx_len"]),
+            ids=T.full((B, S), w.mask_id, dtype=T.int32, device="cuda"),
+            n_masked=T.full((B,), S, dtype=T.int32, device="cuda"),
+            steps=T.zeros(B, dtype=T.int32, device="cuda"),
+            commit_step=T.zeros((B, S), dtype=T.uint8, device="cuda"),
+            y=T.empty((B, S, w.H), dtype=T.int16, device="cuda"),
+            attn_out=T.empty((B, S, w.Hq, w.D), dtype=T.int16, device="cuda"),
+            logits=T.empty((B, S, w.V), dtype=T.float32, device="cuda"),
+            conf=T.empty((B, S), dtype=T.float32, device="cuda"),
+            commit=T.empty((B, S), dtype=T.uint8, device="cuda"))
+        self.desc = tt.step_desc(self.dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps,
+                                 seed, 0, w.logits_kind, w.boost_lo, w.boost_hi)
+        self.ts = tt.step_tensors(**self.t)
+        self.ws = tt.workspace(tt.tt_denoise_workspace(self.desc))
+        ctx = self.inp["ctx_len"].astype(np.int64)
+        self.kv_bytes = int(ctx.sum()) * w.Hkv * w.D * 2 * 2
+        self.attn_bytes = (self.kv_bytes + B * S * w.Hq * w.D * 2 * 2 + B * S * w.Hkv * w.D * 2 * 2)
+        self.attn_flops = 4 * w.Hq * S * w.D * int((ctx + S).sum())
+        self.unmask_bytes_full = B * S * w.V * 4
+
+    def _dev(self, a):
+        a = np.ascontiguousarray(a)
+        T = self.torch
+        return T.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    def reset(self):
+        self.t["ids"].fill_(self.w.mask_id)
+        self.t["n_masked"].fill_(self.w.S)
+        self.t["steps"].zero_()
+        self.t["commit_step"].zero_()
+
+    def block(self, block_index: int):
+        self.desc.logits.block_index = block_index
+        self.tt.tt_denoise_block_loop(self.desc, self.ts, self.ws)
+
+    def step(self, block_index: int):
+        self.desc.logits.block_index = block_index
+        self.tt.tt_denoise_step(self.desc, self.ts, self.ws)
+
+
+def plan_blocks(wb: Workbench, first_block: int, need_steps: int):
+    """Untimed pass: per-block batched step counts (max over sequences) until need_steps."""
+    torch = wb.torch
+    plan, total, bi = [], 0, first_block
+    while total < need_steps:
+        wb.reset()
+        wb.block(bi)
+        torch.cuda.synchronize()
+        n = int(wb.t["steps"].max().item())
+        n = max(n, 1)
+        take = min(n, need_steps - total)
+        plan.append((bi, n, take))
+        total += take
+        bi += 1
+    return plan
+
+
+def run_timed(wb: Workbench, plan, flush, with_events=True):
+    """Runs the plan; returns (elapsed seconds summed over blocks, kernel launches)."""
+    torch = wb.torch
+    elapsed = 0.0
+    launches = 0
+    for bi, n, take in plan:
+        flush()
+        wb.reset()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        if take == n:
+            wb.block(bi)
+            launches += 2 + 6 * n  # dyn-slot write + count, then 6 kernels per step
+        else:
+            for _ in range(take):
+                wb.step(bi)
+            launches += 5 * take
+        e.record()
+        e.synchronize()
+        elapsed += s.elapsed_time(e) / 1e3
+    return elapsed, launches
+
+
+def kernel_times(wb: Workbench, flush, reps: int):
+    """Standalone launches of the attention call and the first-step unmask, L2 flushed first."""
+    tt, torch, w = wb.tt, wb.torch, wb.w
+    B, S = w.B, w.S
+    stream = torch.cuda.current_stream()
+    att_ws = tt.workspace(tt.tt_denoise_attn_workspace(wb.dims))
+    out = torch.empty((B, S, w.Hq, w.D), dtype=torch.int16, device="cuda")
+    um_ws = tt.workspace(tt.tt_confidence_unmask_workspace(B, S, w.V))
+    ids0 = torch.full((B, S), w.mask_id, dtype=torch.int32, device="cuda")
+    ids = ids0.clone()
+    steps = torch.zeros(B, dtype=torch.int32, device="cuda")
+    spec = tt.tt_logits_spec(wb.seed, 0, w.logits_kind, w.boost_lo, w.boost_hi)
+    logits = wb.t["logits"]
+    tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
+    res = {}
+    for name in ("attn", "unmask"):
+        ts = []
+        for r in range(reps + 2):
+            flush()
+            if name == "unmask":
+                ids.copy_(ids0)
+                steps.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            if name == "attn":
+                tt.tt_denoise_attn(wb.dims, wb.t["q"], wb.t["k_blk"], wb.t["v_blk"], wb.t["k_ctx"],
+                                   wb.t["v_ctx"], wb.t["page_table"], wb.t["ctx_len"], out,
+                                   ws=att_ws)
+            else:
+                tt.tt_confidence_unmask(logits, ids, steps, B, S, w.V, w.mask_id, w.gamma,
+                                        w.steps_max, ws=um_ws)
+            e.record(stream)
+            e.synchronize()
+            if r >= 2:
+                ts.append(s.elapsed_time(e) / 1e3)
+        res[name] = statistics.mean(ts)
+    return res
+
+
+def run_e2e(wb: Workbench, plan, torch, tt):
+    """Same plan through the public API with host buffers: every block copies its inputs
+    from pinned host memory and reads back ids/steps/commit_step."""
+    names = ["x", "shift_table", "scale_table", "q", "k_blk", "v_blk", "k_ctx", "v_ctx",
+             "page_table", "ctx_len"]
+    host = {k: torch.empty(wb.t[k].shape, dtype=wb.t[k].dtype, pin_memory=True).copy_(wb.t[k])
+            for k in names if wb.t[k] is not None}
+    ids_h = torch.full(wb.t["ids"].shape, wb.w.mask_id, dtype=torch.int32, pin_memory=True)
+    out_ids = torch.empty_like(ids_h, pin_memory=True)
+    out_steps = torch.empty(wb.t["steps"].shape, dtype=torch.int32, pin_memory=True)
+    out_cs = torch.empty(wb.t["commit_step"].shape, dtype=torch.uint8, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + ids_h.numel() * 4
+    d2h = out_ids.numel() * 4 + out_steps.numel() * 4 + out_cs.numel()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for bi, n, take in plan:
+        for k, v in host.items():
+            wb.t[k].copy_(v, non_blocking=True)
+        wb.t["ids"].copy_(ids_h, non_blocking=True)
+        wb.t["steps"].zero_()
+        wb.t["commit_step"].zero_()
+        if take == n:
+            wb.block(bi)
+        else:
+            wb.t["n_masked"].fill_(wb.w.S)
+            for _ in range(take):
+                wb.step(bi)
+        out_ids.copy_(wb.t["ids"], non_blocking=True)
+        out_steps.copy_(wb.t["steps"], non_blocking=True)
+        out_cs.copy_(wb.t["commit_step"], non_blocking=True)
+    e.record()
+    e.synchronize()
+    return s.elapsed_time(e) / 1e3, h2d, d2h
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_block_time(w: synth.Workload, seed: int, block: int, max_steps=None, b_sample=None):
+    """The oracle decoding one block of the workload on the host cores.
+
+    Returns (denoise steps done, seconds, sample description).  Each step runs the
+    oracle's adaLN, attention (all rows of the sampled sequences), the logits
+    generator for the masked rows and the unmask decision."""
+    import oracle
+    B = w.B if b_sample is None else min(w.B, b_sample)
+    ws = w.replace(B=B)
+    inp = synth.make_attention_inputs(ws, seed)
+    ad = synth.make_adaln_inputs(ws, seed)
+    ids = np.full((B, w.S), w.mask_id, np.int64)
+    steps = np.zeros(B, np.int64)
+    cs = np.zeros((B, w.S), np.uint8)
+    n = 0
+    t0 = time.perf_counter()
+    while np.any(ids == w.mask_id) and (max_steps is None or n < max_steps):
+        nm = (ids == w.mask_id).sum(axis=1)
+        for b in range(B):
+            if nm[b] == 0:
+                continue
+            oracle.adaln_modulate(ad["x"][b], ad["shift_table"][nm[b]], ad["scale_table"][nm[b]],
+                                  w.ln_eps)
+        act = [b for b in range(B) if nm[b] > 0]
+        rows = [(b, s, h) for b in act for s in range(w.S) for h in range(w.Hq)]
+        oracle.denoise_attention_rows(inp, w.softmax_scale, rows)
+        for b in act:
+            pos = np.flatnonzero(ids[b] == w.mask_id)
+            lg = np.zeros((w.S, w.V), np.float32)
+            lg[pos] = synth.logits_rows(seed, b, block, int(steps[b]), pos, w.V, w.mask_id,
+                                        w.logits_kind, w.boost_lo, w.boost_hi)
+            r = oracle.unmask_step(lg, ids[b], int(steps[b]), w.mask_id, w.gamma, w.steps_max, cs[b])
+            ids[b], steps[b], cs[b] = r["ids"], r["steps"], r["commit_step"]
+        n += 1
+    dt = time.perf_counter() - t0
+    return n, dt, B
+
+
+def cpu_baseline(w: synth.Workload, seed: int):
+    budget = 20.0
+    steps = 0
+    secs = 0.0
+    block = 0
+    b_sample = 1 if w.B > 1 else None
+    while secs < budget and block < 64:
+        n, dt, B = oracle_block_time(w, seed, block, b_sample=b_sample)
+        steps += n
+        secs += dt
+        block += 1
+        if secs > budget / 2 and block >= 1:
+            break
+    frac = (B / w.B)
+    # a denoise step of the full batch costs ~1/frac of the sampled one on the CPU
+    value = steps / secs * frac
+    sample = (f"{block} block(s) of {B} of {w.B} sequence(s), {steps} denoise steps, "
+              f"{secs:.1f} s; steps/s scaled by {frac:g} to the full batch")
+    return {"value": value, "unit": "denoise steps/s", "cores": cores_used(), "kind": "oracle",
+            "sample": sample}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workload(args)
+    b_sample = 1 if w.B > 1 else None
+    # warm-up steps
+    done, _, _ = oracle_block_time(w, args.seed, 10_000, max_steps=max(args.warmup, 3), b_sample=b_sample)
+    steps, secs, block = 0, 0.0, 0
+    while steps < args.steps:
+        n, dt, B = oracle_block_time(w, args.seed, block, max_steps=args.steps - steps, b_sample=b_sample)
+        steps += n
+        secs += dt
+        block += 1
+    frac = B / w.B
+    value = steps / secs * frac
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "denoise steps/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "gamma": w.gamma, "bench_step": "one denoise step of the batch"},
+        "cpu_baseline": {"value": value, "unit": "denoise steps/s", "cores": cores_used(),
+                         "kind": "oracle",
+                         "sample": f"{steps} denoise steps over {block} block(s) of {B} of {w.B} "
+                                   f"sequence(s), scaled by {frac:g}"},
+        "e2e": {"value": value, "unit": "denoise steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank, world, local = dist_env()
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from block_wise_mask_tt_b300 import tt
+
+    w = workload(args)
+    seed = args.seed + 1000 * rank
+    wb = Workbench(tt, torch, w, seed)
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+
+    warm = max(args.warmup, 3)
+    warm_plan = plan_blocks(wb, 100_000, warm)
+    plan = plan_blocks(wb, 0, args.steps)
+    total_steps = sum(t for _, _, t in plan)
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        smi_id = str(local)
+
+    with ClockSampler(smi_id) as clk:
+        t_warm = time.time()
+        run_timed(wb, warm_plan, flush)
+        while time.time() - t_warm < args.min_warmup_s:
+            run_timed(wb, warm_plan, flush)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        elapsed, launches = run_timed(wb, plan, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([elapsed], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    status = tt.tt_device_status(True)
+    if status != 0:
+        raise RuntimeError(f"device-side error {status} during the timed region")
+
+    value = world * total_steps / elapsed
+    peaks, peak_kind = load_peaks()
+    ktimes = kernel_times(wb, flush, args.kernel_reps)
+    hbm = peaks["hbm_gbs"]
+    tc = peaks["bf16_tflops"]
+    attn_gbs = wb.attn_bytes / ktimes["attn"] / 1e9
+    attn_tfs = wb.attn_flops / ktimes["attn"] / 1e12
+    attn_bound = "hbm" if wb.attn_bytes / hbm / 1e9 >= wb.attn_flops / tc / 1e12 else "tensor"
+    attn_roof = max(wb.attn_bytes / (hbm * 1e9), wb.attn_flops / (tc * 1e12))
+    um_gbs = wb.unmask_bytes_full / ktimes["unmask"] / 1e9
+    kernels = {
+        "tt_denoise_attn": {"us": ktimes["attn"] * 1e6, "GB_s": attn_gbs, "TFLOP_s": attn_tfs,
+                            "bound": attn_bound, "roofline_us": attn_roof * 1e6,
+                            "frac": attn_roof / ktimes["attn"], "algorithmic_bytes": wb.attn_bytes,
+                            "flops": wb.attn_flops},
+        "tt_confidence_unmask": {"us": ktimes["unmask"] * 1e6, "GB_s": um_gbs,
+                                 "roofline_us": wb.unmask_bytes_full / (hbm * 1e9) * 1e6,
+                                 "frac": um_gbs / hbm, "algorithmic_bytes": wb.unmask_bytes_full},
+    }
+    if ktimes["attn"] >= ktimes["unmask"]:
+        if attn_bound == "hbm":
+            roof = {"kernel": "tt_denoise_attn (split + merge)", "bound": "hbm", "achieved": attn_gbs,
+                    "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm}
+        else:
+            roof = {"kernel": "tt_denoise_attn (split + merge)", "bound": "tensor",
+                    "achieved": attn_tfs, "peak": tc, "unit": "TFLOP/s", "frac": attn_tfs / tc}
+    else:
+        roof = {"kernel": "tt_confidence_unmask (first step, all rows masked)", "bound": "hbm",
+                "achieved": um_gbs, "peak": hbm, "unit": "GB/s", "frac": um_gbs / hbm}
+    roof["traffic"] = None
+    roof["peak_source"] = peak_kind
+
+    e2e = None
+    if not args.no_e2e:
+        e_el, h2d, d2h = run_e2e(wb, plan, torch, tt)
+        if world > 1:
+            t = torch.tensor([e_el], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_el = float(t.item())
+        e2e = {"value": world * total_steps / e_el, "unit": "denoise steps/s",
+               "h2d_bytes_per_step": int(h2d * len(plan) / total_steps),
+               "d2h_bytes_per_step": int(d2h * len(plan) / total_steps)}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, seed)
+    blocks_full = sum(1 for _, n, t in plan if t == n)
+    line = {
+        "metric": METRIC, "value": value, "unit": "denoise steps/s", "n_gpus": world,
+        "steps": total_steps, "warmup": sum(t for _, _, t in warm_plan),
+        "ms_per_step": 1e3 * elapsed / total_steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "D": w.D, "H": w.H, "V": w.V, "gamma": w.gamma, "paged": w.paged,
+                   "bench_step": "one denoise step of the whole batch",
+                   "blocks_timed": len(plan), "whole_blocks": blocks_full,
+                   "tokens_per_step": w.B * w.S * blocks_full / max(1, sum(t for _, n, t in plan if t == n)),
+                   "l2": "flushed (512 MiB write) before every timed block, outside the events",
+                   "parallelism": f"replicas{world}"},
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+// Host-side interface between the C ABI (tt_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tti {
+
+// ----------------------------------------------------------------------------- adaLN
+struct AdalnParams {
+    const uint16_t* x;
+    const float* shift;
+    const float* scale;
+    const int32_t* row_index;   // nullable
+    int table_rows;
+    const int32_t* skip_if_zero;  // nullable: sequences whose entry is 0 are skipped
+    uint16_t* y;
+    int B, S, H;
+    float eps;
+    int* err;
+};
+constexpr int kAdalnMaxH = 8192;
+cudaError_t launch_adaln(const AdalnParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------- logits
+struct LogitsParams {
+    const int32_t* ids;    // nullable
+    const int32_t* steps;  // nullable
+    float* logits;
+    int B, S, V;
+    int32_t mask_id;
+    uint32_t seed;
+    int block_index;
+    int kind;
+    float boost_lo, boost_hi;
+    const uint32_t* dyn;   // nullable: {seed, block_index} read on the device instead
+};
+cudaError_t launch_logits(const LogitsParams& p, cudaStream_t stream);
+cudaError_t launch_set_logits_dyn(uint32_t* dyn, uint32_t seed, int block_index, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------- unmask
+struct UnmaskPartial {
+    float m;    // max logit of the chunk (mask id excluded)
+    float sum;  // sum of exp(logit - m) over the chunk
+    int arg;    // lowest id attaining m
+    int pad;
+};
+struct UnmaskParams {
+    const float* logits;
+    int32_t* ids;
+    int32_t* n_masked;   // nullable
+    int32_t* steps;
+    float* conf;         // nullable
+    uint8_t* commit;     // nullable
+    uint8_t* commit_step;  // nullable
+    int B, S, V;
+    int32_t mask_id;
+    float gamma;
+    int max_steps;
+    int chunk;      // vocabulary entries per CTA (multiple of 1024)
+    int n_chunks;
+    UnmaskPartial* part;     // [B][S][n_chunks]
+    unsigned int* ticket;    // [B], zero on entry, zero on exit
+    int* err;
+};
+size_t unmask_workspace_bytes(int B, int S, int V);
+void unmask_layout(int B, int S, int V, void* ws, UnmaskParams& p);
+cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream);
+
+// -------------------------------------------------------------------------- attention
+struct AttnGeom {
+    int B, S, Hq, Hkv, G, D;
+    int s_per_tile;    // block positions per 128-row tile
+    int rows_per_tile; // s_per_tile * G (<= 128)
+    int n_row_tiles;
+    int R;             // G * S rows per (sequence, kv head)
+    int max_ctx;       // contiguous: token stride; paged: max_pages * page_size
+    int page_size;     // 0 or 64
+    int max_pages, num_pages;
+    int n_splits;
+    int tiles_per_split;  // 64-token tiles per split
+    float scale_log2;     // softmax_scale * log2(e)
+};
+bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_size,
+                   int max_pages, int num_pages, float softmax_scale, int num_splits,
+                   AttnGeom& g, const char** why);
+size_t attn_workspace_bytes(const AttnGeom& g);
+
+struct AttnSplitParams {
+    AttnGeom g;
+    const int32_t* ctx_len;      // nullable (contiguous only)
+    const int32_t* page_table;   // nullable
+    const int32_t* skip_if_zero; // nullable
+    float* part_acc;             // [B][Hkv][n_splits][R][D]
+    float* part_ml;              // [B][Hkv][n_splits][R][2]
+    int* err;
+};
+struct AttnMaps {
+    CUtensorMap q;   // bf16 [B*S][Hq][D], box (64, G, s_per_tile)
+    CUtensorMap k;   // bf16 [rows][Hkv][D], box (64, 1, 64)
+    CUtensorMap v;
+};
+cudaError_t attn_split_prepare(int D);  // sets the kernel's shared-memory limit on this device
+cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cudaStream_t stream);
+
+struct AttnMergeParams {
+    AttnGeom g;
+    const uint16_t* q;
+    const uint16_t* k_blk;
+    const uint16_t* v_blk;
+    const int32_t* ctx_len;
+    const int32_t* skip_if_zero;
+    const float* part_acc;
+    const float* part_ml;
+    uint16_t* out;
+    float* lse;
+    int* err;
+};
+cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------ loop
+struct InitParams {
+    const int32_t* ids;
+    int32_t* n_masked;
+    uint32_t* iter;   // nullable: loop iteration counter, reset to 0
+    int B, S;
+    int32_t mask_id;
+};
+cudaError_t launch_count_masked(const InitParams& p, cudaStream_t stream);
+
+// Sets the block graph's WHILE condition: some sequence still has masked positions
+// and steps left, and fewer than max_steps + 1 iterations have run (a hard cap).
+struct LoopCondParams {
+    const int32_t* n_masked;
+    const int32_t* steps;
+    uint32_t* iter;
+    int B;
+    int max_steps;
+    unsigned long long handle;
+};
+cudaError_t launch_loop_cond(const LoopCondParams& p, cudaStream_t stream);
+
+}  // namespace tti

@@ -1,0 +1,279 @@
+// Confidence unmasking (one denoise step for every sequence of a batch).
+//
+// "Nemotron-Labs-TwoTower" wiki, "Block-wise generation": each step predicts every
+// masked position in parallel, commits those whose confidence clears gamma, keeps a
+// floor so the block completes within T steps; the mask token is never emitted and
+// decoded positions stay fixed.
+//
+// Pass structure: a grid of (vocabulary chunk, position, sequence) CTAs streams the
+// fp32 logits of masked rows once (128-bit loads that bypass L1 and are marked
+// evict-first in L2), reducing each chunk to (max, lowest argmax, sum of exp).  The
+// last CTA of a sequence to finish (atomic ticket after a release fence; nothing
+// spins) merges the chunk partials of its S rows and applies the commit/remask
+// update in place with one warp.
+#include <math_constants.h>
+
+#include "tt_device.cuh"
+#include "tt_internal.h"
+
+namespace tti {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Red {
+    float m;
+    float s;
+    int a;
+};
+
+// Merge two (max, sum-of-exp relative to max, argmax) triples; equal maxima keep
+// the lower id.
+__device__ __forceinline__ Red combine(Red x, Red y) {
+    Red r;
+    r.m = fmaxf(x.m, y.m);
+    if (r.m == -CUDART_INF_F) {
+        r.s = 0.f;
+        r.a = min(x.a, y.a);
+        return r;
+    }
+    r.s = x.s * exp2f((x.m - r.m) * kLog2e) + y.s * exp2f((y.m - r.m) * kLog2e);
+    r.a = (x.m > y.m) ? x.a : (y.m > x.m) ? y.a : min(x.a, y.a);
+    return r;
+}
+
+__device__ __forceinline__ Red warp_combine(Red v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Red w;
+        w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
+        w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
+        w.a = __shfl_xor_sync(0xffffffffu, v.a, o);
+        v = combine(v, w);
+    }
+    return v;
+}
+
+// Folds one batch of values (ids ascending in the order given) into the running
+// triple of this thread.
+template <int N>
+__device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&id)[N]) {
+    float bm = x[0];
+    int ba = id[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+        if (x[i] > bm) {
+            bm = x[i];
+            ba = id[i];
+        }
+    }
+    if (bm > acc.m) {
+        acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - bm) * kLog2e);
+        acc.m = bm;
+        acc.a = ba;
+    }
+    if (acc.m == -CUDART_INF_F) return;
+    const float off = -acc.m * kLog2e;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) s += exp2f(fmaf(x[i], kLog2e, off));
+    acc.s += s;
+}
+
+// Runs on the whole CTA that finished sequence b last.  Every warp merges the chunk
+// partials of some rows (lanes over chunks, so the loads are independent), then warp
+// 0 takes the commit/remask decision for the S <= 32 positions.
+__device__ void decide(const UnmaskParams& p, int b, float* sh_conf, int* sh_tok, int* sh_masked) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int S = p.S;
+    for (int s = warp; s < S; s += kThreads / 32) {
+        const int row = b * S + s;
+        const bool masked = __ldcg(p.ids + row) == p.mask_id;
+        float conf = 0.f;
+        int tok = 0;
+        if (masked) {
+            const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)row * p.n_chunks);
+            Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
+            for (int c = lane; c < p.n_chunks; c += 32) {
+                const float4 v = __ldcg(pp + c);
+                acc = combine(acc, Red{v.x, v.y, __float_as_int(v.z)});
+            }
+            acc = warp_combine(acc);
+            conf = (acc.s > 0.f) ? 1.0f / acc.s : 0.f;
+            tok = acc.a;
+        }
+        if (lane == 0) {
+            sh_conf[s] = conf;
+            sh_tok[s] = tok;
+            sh_masked[s] = masked ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const bool in = lane < S;
+    const int row = b * S + lane;
+    const bool masked = in && sh_masked[lane] != 0;
+    const float conf = in ? sh_conf[lane] : 0.f;
+    const int tok = in ? sh_tok[lane] : 0;
+    const unsigned mball = __ballot_sync(0xffffffffu, masked);
+    const int m = __popc(mball);
+    const int steps_b = __ldcg(p.steps + b);
+    bool take = false;
+    if (m > 0) {
+        const int left = p.max_steps - steps_b;
+        const int k_min = (left > 0) ? (m + left - 1) / left : m;
+        const bool above = masked && conf >= p.gamma;
+        const unsigned aball = __ballot_sync(0xffffffffu, above);
+        if (__popc(aball) >= k_min) {
+            take = above;
+        } else {
+            int rank = 0;
+            for (int j = 0; j < 32; ++j) {
+                const float cj = __shfl_sync(0xffffffffu, conf, j);
+                const bool mj = (mball >> j) & 1u;
+                rank += (mj && (cj > conf || (cj == conf && j < lane))) ? 1 : 0;
+            }
+            take = masked && rank < k_min;
+        }
+    }
+    const int n_take = __popc(__ballot_sync(0xffffffffu, take));
+    if (in) {
+        if (take) {
+            p.ids[row] = tok;
+            if (p.commit_step) p.commit_step[row] = (uint8_t)(steps_b + 1);
+        }
+        if (p.commit) p.commit[row] = take ? 1 : 0;
+        if (p.conf) p.conf[row] = masked ? conf : 0.f;
+    }
+    if (lane == 0) {
+        if (m > 0) p.steps[b] = steps_b + 1;
+        if (p.n_masked) p.n_masked[b] = m - n_take;
+        p.ticket[b] = 0u;
+    }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) unmask_kernel(UnmaskParams p) {
+    const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int row = b * p.S + s;
+    const int tid = threadIdx.x;
+    __shared__ Red red[kThreads / 32];
+    __shared__ int is_last;
+    __shared__ float sh_conf[32];
+    __shared__ int sh_tok[32];
+    __shared__ int sh_masked[32];
+
+    const bool masked = __ldcg(p.ids + row) == p.mask_id;
+    if (masked) {
+        const int v0 = c * p.chunk;
+        const int v1 = min(p.V, v0 + p.chunk);
+        const float* rowp = p.logits + (size_t)row * p.V;
+        const int mid = p.mask_id;
+        Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
+        if (kVec) {
+            // 4 float4 per thread per batch, ids ascending within the batch.
+            const int n4 = (v1 - v0) >> 2;
+            const float4* base = reinterpret_cast<const float4*>(rowp + v0);
+            int f = tid;
+            for (; f + 3 * kThreads < n4; f += 4 * kThreads) {
+                float4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) q[u] = ttk::ld_stream_f4(base + f + u * kThreads);
+                float x[16];
+                int id[16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i0 = v0 + 4 * (f + u * kThreads);
+                    x[4 * u + 0] = q[u].x;
+                    x[4 * u + 1] = q[u].y;
+                    x[4 * u + 2] = q[u].z;
+                    x[4 * u + 3] = q[u].w;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        id[4 * u + e] = i0 + e;
+                        if (i0 + e == mid) x[4 * u + e] = -CUDART_INF_F;
+                    }
+                }
+                fold<16>(acc, x, id);
+            }
+            for (; f < n4; f += kThreads) {
+                const float4 q = ttk::ld_stream_f4(base + f);
+                const int i0 = v0 + 4 * f;
+                float x[4] = {q.x, q.y, q.z, q.w};
+                int id[4] = {i0, i0 + 1, i0 + 2, i0 + 3};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (id[e] == mid) x[e] = -CUDART_INF_F;
+                fold<4>(acc, x, id);
+            }
+        } else {
+            for (int v = v0 + tid; v < v1; v += kThreads) {
+                float x[1] = {__ldcs(rowp + v)};
+                int id[1] = {v};
+                if (v == mid) x[0] = -CUDART_INF_F;
+                fold<1>(acc, x, id);
+            }
+        }
+        acc = warp_combine(acc);
+        if ((tid & 31) == 0) red[tid >> 5] = acc;
+        __syncthreads();
+        if (tid < 32) {
+            Red r = (tid < kThreads / 32) ? red[tid] : Red{-CUDART_INF_F, 0.f, 0x7fffffff};
+            r = warp_combine(r);
+            if (tid == 0) {
+                float4 out;
+                out.x = r.m;
+                out.y = r.s;
+                out.z = __int_as_float(r.a);
+                out.w = 0.f;
+                __stcg(reinterpret_cast<float4*>(p.part + (size_t)row * p.n_chunks + c), out);
+            }
+        }
+    }
+    if (tid == 0) {
+        __threadfence();
+        const unsigned t = atomicAdd(p.ticket + b, 1u);
+        is_last = (t == (unsigned)(p.S * p.n_chunks - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    decide(p, b, sh_conf, sh_tok, sh_masked);
+}
+
+}  // namespace
+
+size_t unmask_workspace_bytes(int B, int S, int V) {
+    // Sized for the smallest chunk (1024 ids), the largest chunk count.
+    const int n_chunks = (V + 1023) / 1024;
+    size_t part = (size_t)B * S * n_chunks * sizeof(UnmaskPartial);
+    part = (part + 255) & ~size_t(255);
+    return part + 256 + (size_t)(B + 1) * sizeof(unsigned int);
+}
+
+void unmask_layout(int B, int S, int V, void* ws, UnmaskParams& p) {
+    // Chunk of 8192 ids (32 KiB of fp32) per CTA; fewer rows get smaller chunks so
+    // that the grid still covers the SMs several times.
+    int chunk = 8192;
+    const long long rows = (long long)B * S;
+    while (chunk > 2048 && rows * ((V + chunk - 1) / chunk) < 148LL * 3) chunk >>= 1;
+    p.chunk = chunk;
+    p.n_chunks = (V + chunk - 1) / chunk;
+    p.part = reinterpret_cast<UnmaskPartial*>(ws);
+    size_t part = (size_t)B * S * ((V + 1023) / 1024) * sizeof(UnmaskPartial);
+    part = (part + 255) & ~size_t(255);
+    p.ticket = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) + part);
+}
+
+cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
+    dim3 grid(p.n_chunks, p.S, p.B);
+    if ((p.V & 3) == 0)
+        unmask_kernel<true><<<grid, kThreads, 0, stream>>>(p);
+    else
+        unmask_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace tti

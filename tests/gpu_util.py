@@ -1,0 +1,137 @@
+"""Helpers shared by the GPU parity tests: device transfer and the comparison rules.
+
+Comparison rules (tolerances of the parity contract):
+* attention output: max |gpu - oracle| <= 1e-2 and ||gpu - oracle||_2 / ||oracle||_2 <= 5e-3
+  against the fp64 oracle on the same bf16 inputs; lse within 4e-3 (natural log) -
+  the kernel normalises with the bf16-rounded probabilities it multiplies V with, whose
+  relative rounding error is at most 2^-9 per term;
+* adaLN: within one bf16 ulp of the unrounded fp64 value (the kernel's fp32 statistics
+  are ~1e-6 relative, so the only visible difference is the final rounding);
+* unmask: token ids, commit masks, step counts bit-exact, except sequences in which a
+  masked position's oracle confidence lies within 1e-5 of gamma, or in which the floor
+  decides between confidences within 1e-5 (relative) of each other - those are counted
+  and checked for validity only; confidences within 1e-5 relative.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+
+ATTN_MAX_ABS = 1e-2
+ATTN_REL_L2 = 5e-3
+LSE_ABS = 4e-3
+CONF_REL = 1e-5
+GAMMA_BAND = 1e-5
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    a = t.detach().cpu().contiguous()
+    if a.dtype in (torch.int16, torch.bfloat16):
+        return a.view(torch.int16).numpy().view(np.uint16)
+    return a.numpy()
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def check_attention(O_gpu: np.ndarray, O_ref: np.ndarray, lse_gpu=None, lse_ref=None, what=""):
+    err = np.abs(O_gpu - O_ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    rel = float(np.linalg.norm(O_gpu - O_ref) / max(np.linalg.norm(O_ref), 1e-30))
+    assert max_abs <= ATTN_MAX_ABS, f"{what}: max abs err {max_abs}"
+    assert rel <= ATTN_REL_L2, f"{what}: rel L2 err {rel}"
+    if lse_gpu is not None:
+        lerr = float(np.abs(lse_gpu - lse_ref).max())
+        assert lerr <= LSE_ABS, f"{what}: lse err {lerr}"
+    return max_abs, rel
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def oracle_unmask_batch(logits, ids0, steps0, cs0, mask_id, gamma, T):
+    B = ids0.shape[0]
+    out = []
+    for b in range(B):
+        out.append(oracle.unmask_step(logits[b], ids0[b], int(steps0[b]), mask_id, gamma, T, cs0[b]))
+    return out
+
+
+def ambiguous(r: dict, ids0_b: np.ndarray, mask_id: int, gamma: float) -> bool:
+    masked = np.flatnonzero(ids0_b == mask_id)
+    if masked.size == 0:
+        return False
+    conf = r["conf"][masked]
+    if np.any(np.abs(conf - gamma) <= GAMMA_BAND):
+        return True
+    n_above = int(np.sum(conf >= gamma))
+    k = r["k_min"]
+    if n_above < k < masked.size:
+        srt = np.sort(conf)[::-1]
+        if abs(srt[k - 1] - srt[k]) <= GAMMA_BAND * srt[k - 1]:
+            return True
+    return False
+
+
+def compare_unmask(gpu: dict, ora: list, ids0, steps0, mask_id, gamma, what="") -> int:
+    """Asserts parity of one unmask call for a batch; returns the number of excluded sequences."""
+    excluded = 0
+    B = ids0.shape[0]
+    for b in range(B):
+        r = ora[b]
+        masked = ids0[b] == mask_id
+        cg = gpu["conf"][b]
+        co = r["conf"]
+        assert np.all(cg[~masked] == 0.0), f"{what} b={b}: conf of unmasked position not 0"
+        if masked.any():
+            rel = np.abs(cg[masked] - co[masked]) / np.maximum(co[masked], 1e-300)
+            assert rel.max() <= CONF_REL, f"{what} b={b}: conf rel err {rel.max()}"
+        if ambiguous(r, ids0[b], mask_id, gamma):
+            excluded += 1
+            # validity only: committed tokens are the oracle's argmax, decoded positions
+            # unchanged, one step taken, counts consistent
+            com = gpu["commit"][b].astype(bool)
+            assert np.all(~com | masked)
+            assert np.array_equal(gpu["ids"][b][com], r["tok"][com])
+            assert np.array_equal(gpu["ids"][b][~masked], ids0[b][~masked])
+            assert np.all(gpu["ids"][b][masked & ~com] == mask_id)
+            assert gpu["steps"][b] == r["steps"]
+            assert com.sum() >= r["k_min"]
+            continue
+        assert np.array_equal(gpu["ids"][b], r["ids"]), f"{what} b={b}: ids differ"
+        assert np.array_equal(gpu["commit"][b], r["commit"]), f"{what} b={b}: commit differs"
+        assert gpu["steps"][b] == r["steps"], f"{what} b={b}: steps differ"
+        assert gpu["n_masked"][b] == r["n_masked"], f"{what} b={b}: n_masked differs"
+        assert np.array_equal(gpu["commit_step"][b], r["commit_step"]), f"{what} b={b}: commit_step"
+    return excluded
+
+
+def run_unmask(tt, logits: np.ndarray, ids0, steps0, cs0, mask_id, gamma, T):
+    B, S, V = logits.shape
+    d_logits = dev(logits.astype(np.float32))
+    ids = dev(ids0.astype(np.int32))
+    steps = dev(steps0.astype(np.int32))
+    cs = dev(cs0.astype(np.uint8))
+    n_masked = torch.zeros(B, dtype=torch.int32, device="cuda")
+    conf = torch.full((B, S), -1.0, dtype=torch.float32, device="cuda")
+    commit = torch.full((B, S), 7, dtype=torch.uint8, device="cuda")
+    tt.tt_confidence_unmask(d_logits, ids, steps, B, S, V, mask_id, gamma, T, n_masked=n_masked,
+                            conf=conf, commit=commit, commit_step=cs)
+    torch.cuda.synchronize()
+    return dict(ids=host(ids), steps=host(steps), n_masked=host(n_masked), conf=host(conf),
+                commit=host(commit), commit_step=host(cs))

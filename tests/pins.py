@@ -9,7 +9,6 @@ layer_norm, scipy softmax), closed forms, invariants and special cases.
 import math
 
 import numpy as np
-import scipy.special
 import torch
 import torch.nn.functional as F
 
@@ -207,6 +206,7 @@ def check_conf_two_valued(row_conf_fn):
 
 
 def check_conf_vs_scipy(row_conf_fn):
+    import scipy.special
     rng = np.random.default_rng(5)
     for V in (8, 1000, 131072):
         for mask in (3, 0, V - 1):

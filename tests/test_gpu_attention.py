@@ -1,0 +1,138 @@
+"""tt_denoise_attn against the fp64 oracle: contiguous and paged caches, GQA packing,
+ragged tails, several row tiles and KV tiles, split invariance, empty contexts."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_wise_mask_tt_b300 import synth
+from gpu_util import bf16_to_f64, check_attention, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tt():
+    from block_wise_mask_tt_b300 import tt as _tt
+    return _tt
+
+
+def run_attn(tt, w, inp, num_splits=0):
+    B, S, Hq, Hkv, D = w.B, w.S, w.Hq, w.Hkv, w.D
+    if w.paged:
+        kp, vp = inp["k_pages"], inp["v_pages"]
+        dims = tt.attn_dims(B, S, Hq, Hkv, D, 0, w.page_size, inp["page_table"].shape[1], kp.shape[0],
+                            w.softmax_scale, num_splits)
+        kc, vc, pt = dev(kp), dev(vp), dev(inp["page_table"])
+    else:
+        L = inp["k_ctx"].shape[1]
+        dims = tt.attn_dims(B, S, Hq, Hkv, D, L, 0, 0, 0, w.softmax_scale, num_splits)
+        kc = dev(inp["k_ctx"]) if L else None
+        vc = dev(inp["v_ctx"]) if L else None
+        pt = None
+    out = torch.full((B, S, Hq, D), 0x7FC0, dtype=torch.int16, device="cuda")  # NaN pattern
+    lse = torch.full((B, S, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    tt.tt_denoise_attn(dims, dev(inp["q"]), dev(inp["k_blk"]), dev(inp["v_blk"]), kc, vc, pt,
+                       dev(inp["ctx_len"]), out, lse)
+    torch.cuda.synchronize()
+    assert tt.tt_device_status(True) == 0
+    return bf16_to_f64(host(out)), host(lse).astype(np.float64)
+
+
+def W(**kw):
+    base = dict(name="t", B=1, L=256, S=16, Hq=4, Hkv=1, D=64, H=256, V=1024)
+    base.update(kw)
+    return synth.Workload(**base)
+
+
+CASES = {
+    "c0_shape": W(softmax_scale=1 / 8.0, qkv_fp32_source=True),
+    "g16_d128_L300": W(B=2, L=300, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128)),
+    "g16_d128_s32_ragged": W(B=3, L=200, L_min=1, S=32, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128)),
+    "g4_d64_L1000": W(B=2, L=1000, S=16, Hq=8, Hkv=2, D=64, softmax_scale=0.125),
+    "g12_d128_s13": W(B=2, L=130, S=13, Hq=24, Hkv=2, D=128, softmax_scale=0.09),
+    "g1_d64_s1": W(B=3, L=70, S=1, Hq=2, Hkv=2, D=64, softmax_scale=0.125),
+    "g32_d64_s16": W(B=1, L=513, S=16, Hq=32, Hkv=1, D=64, softmax_scale=0.125),
+    "paged_g16_s32": W(B=4, L=700, L_min=1, S=32, Hq=32, Hkv=2, D=128, paged=True,
+                       q_prescale=1 / math.sqrt(128)),
+    "paged_g4_d64": W(B=3, L=300, L_min=1, S=16, Hq=8, Hkv=2, D=64, paged=True, softmax_scale=0.125),
+    "empty_ctx": W(B=2, L=0, S=16, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128)),
+    "large_logits": W(B=1, L=640, S=16, Hq=16, Hkv=1, D=128, softmax_scale=1.0, qkv_std=2.5),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_attention_matches_oracle(tt, name):
+    w = CASES[name]
+    inp = synth.make_attention_inputs(w, seed=len(name))
+    O, lse = run_attn(tt, w, inp)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr, what=name)
+
+
+def test_context_length_zero_for_some_sequences(tt):
+    w = W(B=3, L=256, S=16, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128))
+    inp = synth.make_attention_inputs(w, seed=3, ctx_len=np.array([0, 256, 65], np.int32))
+    O, lse = run_attn(tt, w, inp)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 0])
+def test_split_invariance(tt, splits):
+    w = W(B=2, L=1024, S=16, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128))
+    inp = synth.make_attention_inputs(w, seed=11)
+    O, lse = run_attn(tt, w, inp, num_splits=splits)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr, what=f"splits={splits}")
+
+
+def test_paged_equals_contiguous(tt):
+    w = W(B=3, L=500, L_min=1, S=16, Hq=32, Hkv=2, D=128, paged=True, q_prescale=1 / math.sqrt(128))
+    inp = synth.make_attention_inputs(w, seed=12)
+    Op, lp = run_attn(tt, w, inp, num_splits=2)
+    L = 512
+    kc = np.zeros((w.B, L, w.Hkv, w.D), np.uint16)
+    vc = np.zeros((w.B, L, w.Hkv, w.D), np.uint16)
+    for b in range(w.B):
+        n = int(inp["ctx_len"][b])
+        t = np.arange(n)
+        kc[b, :n] = inp["k_pages"][inp["page_table"][b, t // 64], t % 64]
+        vc[b, :n] = inp["v_pages"][inp["page_table"][b, t // 64], t % 64]
+    inp_c = dict(q=inp["q"], k_blk=inp["k_blk"], v_blk=inp["v_blk"], ctx_len=inp["ctx_len"], k_ctx=kc,
+                 v_ctx=vc)
+    Oc, lc = run_attn(tt, w.replace(paged=False), inp_c, num_splits=2)
+    np.testing.assert_array_equal(Op, Oc)
+    np.testing.assert_array_equal(lp, lc)
+
+
+def test_block_permutation_equivariance(tt):
+    w = W(B=1, L=256, S=16, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128))
+    inp = synth.make_attention_inputs(w, seed=13)
+    O, _ = run_attn(tt, w, inp)
+    perm = np.random.default_rng(0).permutation(16)
+    inp2 = dict(inp)
+    for k in ("q", "k_blk", "v_blk"):
+        inp2[k] = np.ascontiguousarray(inp[k][:, perm])
+    O2, _ = run_attn(tt, w, inp2)
+    np.testing.assert_allclose(O2, O[:, perm], atol=2e-2, rtol=0)
+
+
+def test_bad_page_id_is_reported(tt):
+    w = W(B=2, L=200, L_min=1, S=16, Hq=8, Hkv=2, D=64, paged=True, softmax_scale=0.125)
+    inp = synth.make_attention_inputs(w, seed=14)
+    inp["page_table"][1, 0] = 10 ** 6
+    kp = inp["k_pages"]
+    dims = tt.attn_dims(w.B, w.S, w.Hq, w.Hkv, w.D, 0, 64, inp["page_table"].shape[1], kp.shape[0],
+                        w.softmax_scale, 0)
+    out = torch.zeros((w.B, w.S, w.Hq, w.D), dtype=torch.int16, device="cuda")
+    assert tt.tt_device_status(True) == 0
+    tt.tt_denoise_attn(dims, dev(inp["q"]), dev(inp["k_blk"]), dev(inp["v_blk"]), dev(kp),
+                       dev(inp["v_pages"]), dev(inp["page_table"]), dev(inp["ctx_len"]), out)
+    assert tt.tt_device_status(True) == tt.TT_ERR_DEVICE
+    # sequence 0 is unaffected
+    Or, _ = oracle.denoise_attention({k: (v[:1] if k in ("q", "k_blk", "v_blk", "ctx_len", "page_table")
+                                          else v) for k, v in inp.items()}, w.softmax_scale)
+    check_attention(bf16_to_f64(host(out))[:1], Or)

@@ -2,12 +2,12 @@
 import numpy as np
 import pytest
 import torch
-from sklearn.utils import murmurhash3_32
 
 from block_wise_mask_tt_b300 import synth
 
 
 def test_murmur3_matches_sklearn():
+    murmurhash3_32 = pytest.importorskip("sklearn.utils").murmurhash3_32
     rng = np.random.default_rng(0)
     keys = rng.integers(0, 2 ** 32, size=4096, dtype=np.uint64)
     seeds = rng.integers(0, 2 ** 32, size=64, dtype=np.uint64)
