@@ -53,6 +53,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.5,
                     help="keep warming up for at least this long so the clock sampler sees load")
+    ap.add_argument("--kernel-only", choices=("attn", "unmask", "adaln", "logits", "step"),
+                    default=None,
+                    help="profiling aid: run only --reps standalone calls of one entry point on "
+                         "the workload (after 3 untimed ones) and print their mean time")
+    ap.add_argument("--reps", type=int, default=3)
     return ap.parse_args()
 
 
@@ -289,6 +294,54 @@ def kernel_times(wb: Workbench, flush, reps: int):
     return res
 
 
+def kernel_only(wb: Workbench, which: str, reps: int):
+    """Standalone calls of one entry point, for profiler captures (no JSON bench line)."""
+    tt, torch, w = wb.tt, wb.torch, wb.w
+    B, S = w.B, w.S
+    att_ws = tt.workspace(tt.tt_denoise_attn_workspace(wb.dims))
+    out = torch.empty((B, S, w.Hq, w.D), dtype=torch.int16, device="cuda")
+    um_ws = tt.workspace(tt.tt_confidence_unmask_workspace(B, S, w.V))
+    ids0 = torch.full((B, S), w.mask_id, dtype=torch.int32, device="cuda")
+    ids = ids0.clone()
+    steps = torch.zeros(B, dtype=torch.int32, device="cuda")
+    spec = tt.tt_logits_spec(wb.seed, 0, w.logits_kind, w.boost_lo, w.boost_hi)
+    logits = wb.t["logits"]
+    tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
+    y = torch.empty((B, S, w.H), dtype=torch.int16, device="cuda")
+
+    def call():
+        if which == "attn":
+            tt.tt_denoise_attn(wb.dims, wb.t["q"], wb.t["k_blk"], wb.t["v_blk"], wb.t["k_ctx"],
+                               wb.t["v_ctx"], wb.t["page_table"], wb.t["ctx_len"], out, ws=att_ws)
+        elif which == "unmask":
+            ids.copy_(ids0)
+            steps.zero_()
+            tt.tt_confidence_unmask(logits, ids, steps, B, S, w.V, w.mask_id, w.gamma,
+                                    w.steps_max, ws=um_ws)
+        elif which == "adaln":
+            tt.tt_adaln_modulate(wb.t["x"], wb.t["shift_table"], wb.t["scale_table"], y,
+                                 eps=w.ln_eps, row_index=wb.t["n_masked"], table_rows=S + 1)
+        elif which == "logits":
+            tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
+        else:
+            wb.reset()
+            wb.step(0)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        call()
+    e.record()
+    e.synchronize()
+    if tt.tt_device_status(True) != 0:
+        raise RuntimeError("device-side error reported")
+    print(json.dumps({"kernel_only": which, "workload": w.name, "reps": reps,
+                      "us_per_call_back_to_back": s.elapsed_time(e) * 1e3 / reps}), flush=True)
+
+
 def run_e2e(wb: Workbench, plan, torch, tt):
     """Same plan through the public API with host buffers: every block copies its inputs
     from pinned host memory and reads back ids/steps/commit_step."""
@@ -435,6 +488,9 @@ def main():
     w = workload(args)
     seed = args.seed + 1000 * rank
     wb = Workbench(tt, torch, w, seed)
+    if args.kernel_only:
+        kernel_only(wb, args.kernel_only, args.reps)
+        return
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
 
     def flush():

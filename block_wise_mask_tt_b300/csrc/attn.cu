@@ -269,6 +269,19 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                 make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         l_run += lsum;
+        if (lim < kTileKeys) {
+            // Last tile of a context that ends inside it: the V rows past the end are
+            // whatever the cache holds there (another sequence, an unused page slot).
+            // P is 0 for them, but 0 * NaN would still poison O, so zero those rows.
+            constexpr int kChunksPerRow = NP * 8;  // 16-byte chunks per V row
+            uint8_t* vst = smem + L::kV + stage * L::kStage;
+            for (int i = tid; i < (kTileKeys - lim) * kChunksPerRow; i += kSplitThreads) {
+                const int key = lim + i / kChunksPerRow;
+                const int ch = i % kChunksPerRow;
+                *reinterpret_cast<uint4*>(vst + (ch >> 3) * L::kKVPart + key * 128 + ((ch & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         ttk::fence_proxy_async_smem();
         ttk::tc_fence_before();
         __syncthreads();
@@ -294,29 +307,24 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
     }
 
     if (ok) {
-        if (row_valid) {
-            float* acc = p.part_acc + pidx * D;
+        // tcgen05.ld is warp-collective: every lane loads, only rows in range store.
+        float* acc = p.part_acc + pidx * D;
 #pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-                uint32_t o[32];
-                ttk::tmem_ld32(tO + lane_off + cc, o);
-                ttk::tmem_ld_wait32(o);
+        for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            ttk::tmem_ld32(tO + lane_off + cc, o);
+            ttk::tmem_ld_wait32(o);
+            if (row_valid) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
                     *reinterpret_cast<float4*>(acc + cc + e) =
                         make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
                                     __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
             }
+        }
+        if (row_valid) {
             p.part_ml[2 * pidx + 0] = m_run;
             p.part_ml[2 * pidx + 1] = l_run;
-        } else {
-            // tcgen05.ld is warp-collective: lanes without a row still take part.
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-                uint32_t o[32];
-                ttk::tmem_ld32(tO + lane_off + cc, o);
-                ttk::tmem_ld_wait32(o);
-            }
         }
     } else {
         if (tid == 0) ttk::report_error(p.err, ttk::kErrTimeout);

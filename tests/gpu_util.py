@@ -5,8 +5,10 @@ Comparison rules (tolerances of the parity contract):
   against the fp64 oracle on the same bf16 inputs; lse within 4e-3 (natural log) -
   the kernel normalises with the bf16-rounded probabilities it multiplies V with, whose
   relative rounding error is at most 2^-9 per term;
-* adaLN: within one bf16 ulp of the unrounded fp64 value (the kernel's fp32 statistics
-  are ~1e-6 relative, so the only visible difference is the final rounding);
+* adaLN: within one bf16 ulp of the unrounded fp64 value plus 2^-16 of the magnitude
+  of the two terms that are added, |LN(x)*(1+scale)| + |shift|: the kernel's fp32
+  statistics carry a relative error of order sqrt(H) * 2^-24, and where the two terms
+  nearly cancel that absolute error survives in a result far smaller than either;
 * unmask: token ids, commit masks, step counts bit-exact, except sequences in which a
   masked position's oracle confidence lies within 1e-5 of gamma, or in which the floor
   decides between confidences within 1e-5 (relative) of each other - those are counted
@@ -46,16 +48,30 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
-def check_attention(O_gpu: np.ndarray, O_ref: np.ndarray, lse_gpu=None, lse_ref=None, what=""):
+def check_attention(O_gpu: np.ndarray, O_ref: np.ndarray, lse_gpu=None, lse_ref=None, what="",
+                    out_rounding=False):
+    """out_rounding: also allow half a bf16 ulp of the reference per element.  The
+    output is stored in bf16, so where |O| >= 4 (inputs with std > 1) rounding alone
+    can exceed the flat max-abs bound; the N(0,1) workloads never need it."""
     err = np.abs(O_gpu - O_ref)
     max_abs = float(err.max()) if err.size else 0.0
     rel = float(np.linalg.norm(O_gpu - O_ref) / max(np.linalg.norm(O_ref), 1e-30))
-    assert max_abs <= ATTN_MAX_ABS, f"{what}: max abs err {max_abs}"
+    if out_rounding:
+        excess = err - 0.5 * bf16_ulp(O_ref)
+        assert float(excess.max()) <= ATTN_MAX_ABS, f"{what}: max abs err beyond rounding {excess.max()}"
+    else:
+        assert max_abs <= ATTN_MAX_ABS, f"{what}: max abs err {max_abs}"
     assert rel <= ATTN_REL_L2, f"{what}: rel L2 err {rel}"
     if lse_gpu is not None:
         lerr = float(np.abs(lse_gpu - lse_ref).max())
         assert lerr <= LSE_ABS, f"{what}: lse err {lerr}"
     return max_abs, rel
+
+
+def adaln_tol(ref: np.ndarray, shift: np.ndarray) -> np.ndarray:
+    """Allowed |gpu - oracle| for adaLN outputs (see the module docstring)."""
+    terms = np.abs(ref - shift) + np.abs(shift)
+    return bf16_ulp(ref) + 2.0 ** -16 * terms + 1e-30
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:

@@ -1,11 +1,11 @@
-"""tt_adaln_modulate against the fp64 oracle (within one bf16 ulp)."""
+"""tt_adaln_modulate against the fp64 oracle (one bf16 ulp plus the fp32 statistics error)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from block_wise_mask_tt_b300 import synth
-from gpu_util import bf16_to_f64, bf16_ulp, dev, host
+from gpu_util import adaln_tol, bf16_to_f64, bf16_ulp, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -16,10 +16,11 @@ def tt():
     return _tt
 
 
-def _check(y_bits, ref):
+def _check(y_bits, ref, shift):
     got = bf16_to_f64(y_bits)
     err = np.abs(got - ref)
-    assert np.all(err <= bf16_ulp(ref) + 1e-30), float((err / bf16_ulp(ref)).max())
+    tol = adaln_tol(ref, np.broadcast_to(shift, ref.shape))
+    assert np.all(err <= tol), float((err / tol).max())
 
 
 @pytest.mark.parametrize("B,S,H", [(1, 16, 256), (1, 16, 2688), (4, 32, 2688), (3, 5, 8), (2, 3, 8192)])
@@ -30,7 +31,7 @@ def test_adaln_per_sequence(tt, B, S, H):
     tt.tt_adaln_modulate(dev(a["x"]), dev(a["shift"]), dev(a["scale"]), y, eps=1e-5)
     torch.cuda.synchronize()
     ref = oracle.adaln_modulate(a["x"], a["shift"][:, None, :], a["scale"][:, None, :], 1e-5)
-    _check(host(y), ref)
+    _check(host(y), ref, a["shift"][:, None, :])
 
 
 def test_adaln_table_rows(tt):
@@ -44,7 +45,7 @@ def test_adaln_table_rows(tt):
     torch.cuda.synchronize()
     ref = oracle.adaln_modulate(a["x"], a["shift_table"][rows][:, None, :],
                                 a["scale_table"][rows][:, None, :], 1e-5)
-    _check(host(y), ref)
+    _check(host(y), ref, a["shift_table"][rows][:, None, :])
 
 
 def test_adaln_constant_row_and_scale(tt):
@@ -59,7 +60,8 @@ def test_adaln_constant_row_and_scale(tt):
     got = bf16_to_f64(host(y))
     # constant rows give exactly shift (rounded to bf16)
     np.testing.assert_array_equal(got[0, 0], bf16_to_f64(synth.f32_to_bf16_bits(shift[0])))
-    _check(host(y), oracle.adaln_modulate(x, shift[:, None, :], scale[:, None, :], 1e-5))
+    _check(host(y), oracle.adaln_modulate(x, shift[:, None, :], scale[:, None, :], 1e-5),
+           shift[:, None, :])
 
 
 def test_adaln_bad_table_row_is_reported(tt):

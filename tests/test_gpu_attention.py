@@ -69,7 +69,7 @@ def test_attention_matches_oracle(tt, name):
     inp = synth.make_attention_inputs(w, seed=len(name))
     O, lse = run_attn(tt, w, inp)
     Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
-    check_attention(O, Or, lse, lr, what=name)
+    check_attention(O, Or, lse, lr, what=name, out_rounding=w.qkv_std > 1.0)
 
 
 def test_context_length_zero_for_some_sequences(tt):
