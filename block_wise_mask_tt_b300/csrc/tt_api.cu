@@ -597,6 +597,50 @@ tt_status tt_confidence_unmask(const float* logits, int32_t* ids, int32_t* n_mas
     return TT_OK;
 }
 
+tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids, int32_t* n_masked,
+                                       int32_t* steps, float* conf, uint8_t* commit,
+                                       uint8_t* commit_step, int B, int S, int V, int32_t mask_id,
+                                       float gamma, int max_steps, tt_stream_t stream) {
+    TT_TRY(check_vocab(B, S, V));
+    if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
+    if (max_steps < 1 || max_steps > 255) return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
+    if (gamma != gamma) return fail(TT_ERR_INVALID_ARG, "gamma is NaN");
+    TT_TRY(need_ptr(logits, "logits"));
+    TT_TRY(need_ptr(ids, "ids", false));
+    TT_TRY(need_ptr(steps, "steps", false));
+    const size_t need = tti::unmask_workspace_bytes(B, S, V);
+    if (need > tti::kUnmaskNoallocScratchBytes)
+        return fail(TT_ERR_UNSUPPORTED,
+                    "B=%d, S=%d, V=%d needs %zu bytes of scratch; the fixed scratch of "
+                    "tt_confidence_unmask_noalloc holds %zu (use tt_confidence_unmask with a workspace)",
+                    B, S, V, need, tti::kUnmaskNoallocScratchBytes);
+    int* err = nullptr;
+    TT_TRY(device_err_word(&err));
+    void* scratch = nullptr;
+    TT_CUDA(tti::unmask_noalloc_scratch(&scratch));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    tti::UnmaskParams p;
+    p.logits = logits;
+    p.ids = ids;
+    p.n_masked = n_masked;
+    p.steps = steps;
+    p.conf = conf;
+    p.commit = commit;
+    p.commit_step = commit_step;
+    p.B = B;
+    p.S = S;
+    p.V = V;
+    p.mask_id = mask_id;
+    p.gamma = gamma;
+    p.max_steps = max_steps;
+    tti::unmask_layout(B, S, V, scratch, p);
+    p.err = err;
+    // The array keeps whatever the previous call left; the tickets must start at zero.
+    TT_CUDA(cudaMemsetAsync(p.ticket, 0, (size_t)(B + 1) * sizeof(unsigned int), st));
+    TT_CUDA(tti::launch_unmask(p, st));
+    return TT_OK;
+}
+
 size_t tt_denoise_workspace(const tt_step_desc* desc) {
     StepPlan sp;
     if (plan_step(desc, sp) != TT_OK) return 0;

@@ -68,6 +68,11 @@ struct UnmaskParams {
 size_t unmask_workspace_bytes(int B, int S, int V);
 void unmask_layout(int B, int S, int V, void* ws, UnmaskParams& p);
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream);
+// Fixed scratch of tt_confidence_unmask_noalloc (a file-scope __device__ array):
+// unmask_workspace_bytes(B, S, V) must not exceed this.
+constexpr size_t kUnmaskNoallocScratchBytes = size_t(8) << 20;
+// Device address of that array on the current device (looked up once per device).
+cudaError_t unmask_noalloc_scratch(void** out);
 
 // -------------------------------------------------------------------------- attention
 struct AttnGeom {

@@ -13,6 +13,8 @@
 // update in place with one warp.
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "tt_device.cuh"
 #include "tt_internal.h"
 
@@ -274,6 +276,43 @@ cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
     else
         unmask_kernel<false><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace tti
+
+namespace tti {
+
+// ---------------------------------------------------------------------------------
+// Fixed device scratch for tt_confidence_unmask_noalloc.
+//
+// Some callers cannot hand the library a workspace: their device memory belongs to
+// another allocator, or the calling code may not allocate at all.  For them the
+// chunk partials and per-sequence tickets live in this file-scope array instead.
+// It is part of the module image, so every device that loads the library holds it
+// until the process exits, and every call on a device shares it.
+// ---------------------------------------------------------------------------------
+namespace {
+static __device__ __align__(256) unsigned char g_unmask_noalloc_scratch[kUnmaskNoallocScratchBytes];
+}  // namespace
+
+cudaError_t unmask_noalloc_scratch(void** out) {
+    // In host code the array's name is only a host-side stand-in; the kernel needs
+    // its device address, looked up once per device with that device current.
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_unmask_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace tti

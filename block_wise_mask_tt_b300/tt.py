@@ -81,6 +81,8 @@ _SIGS = {
     "tt_confidence_unmask_workspace": (ctypes.c_size_t, [_I, _I, _I]),
     "tt_confidence_unmask": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
                                   ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+    "tt_confidence_unmask_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
+                                          ctypes.c_float, _I, _P]),
     "tt_denoise_workspace": (ctypes.c_size_t, [ctypes.POINTER(tt_step_desc)]),
     "tt_denoise_step": (_I, [ctypes.POINTER(tt_step_desc), ctypes.POINTER(tt_step_tensors), _P,
                              ctypes.c_size_t, _P]),
@@ -202,6 +204,19 @@ def tt_confidence_unmask(logits, ids, steps, B, S, V, mask_id, gamma, max_steps,
         _ptr(conf, "conf", _F32, B * S), _ptr(commit, "commit", _U8, B * S),
         _ptr(commit_step, "commit_step", _U8, B * S), B, S, V, int(mask_id), float(gamma),
         int(max_steps), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def tt_confidence_unmask_noalloc(logits, ids, steps, B, S, V, mask_id, gamma, max_steps,
+                                 n_masked=None, conf=None, commit=None, commit_step=None,
+                                 stream=None) -> None:
+    """tt_confidence_unmask without a workspace: the library's fixed device scratch is
+    used instead (for callers that cannot allocate; calls must not overlap)."""
+    _check(lib.tt_confidence_unmask_noalloc(
+        _ptr(logits, "logits", _F32, B * S * V), _ptr(ids, "ids", _I32, B * S),
+        _ptr(n_masked, "n_masked", _I32, B), _ptr(steps, "steps", _I32, B),
+        _ptr(conf, "conf", _F32, B * S), _ptr(commit, "commit", _U8, B * S),
+        _ptr(commit_step, "commit_step", _U8, B * S), B, S, V, int(mask_id), float(gamma),
+        int(max_steps), _stream(stream)))
 
 
 def step_desc(attn: tt_attn_dims, H, V, mask_id, gamma, max_steps, ln_eps, seed, block_index,

@@ -205,6 +205,38 @@ TT_API tt_status tt_confidence_unmask(const float* logits, int32_t* ids, int32_t
                                size_t workspace_bytes, tt_stream_t stream);
 
 /* --------------------------------------------------------------------------------
+ * tt_confidence_unmask_noalloc: the same confidence-unmasking step, for callers that
+ * cannot provide a workspace.  The pages describing the method have no counterpart
+ * to this entry point; it exists for callers whose device memory is owned entirely
+ * by another allocator (a serving engine that reserves nearly all HBM up front and
+ * hands out only its own buffers) and for code that must not allocate on its hot
+ * path (cudaMalloc can synchronise the device and has no latency bound).
+ *
+ * Arguments, layouts, outputs and errors are those of tt_confidence_unmask without
+ * the workspace.  Instead of a workspace it uses a fixed scratch array of 8 MiB
+ * (a file-scope __device__ array of the library): every device that loads the
+ * library holds those 8 MiB until the process exits.  Sizes whose scratch,
+ * tt_confidence_unmask_workspace(B, S, V), exceeds 8 MiB are rejected with
+ * TT_ERR_UNSUPPORTED before anything is launched (B*S*ceil(V/1024) up to about
+ * 524000, e.g. B*S = 2048 rows at V = 131072 fits).
+ *
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  It clears the part of the scratch that must start at zero with
+ * cudaMemsetAsync on `stream`, then launches the kernel.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture begins.
+ * Every call on a device shares the one array, which keeps the previous call's
+ * contents: calls that may overlap on the GPU (other streams, other host threads)
+ * race with one another and must be ordered by the caller.
+ * -------------------------------------------------------------------------------- */
+TT_API tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids,
+                                              int32_t* n_masked, int32_t* steps, float* conf,
+                                              uint8_t* commit, uint8_t* commit_step, int B,
+                                              int S, int V, int32_t mask_id, float gamma,
+                                              int max_steps, tt_stream_t stream);
+
+/* --------------------------------------------------------------------------------
  * Whole denoise step and whole block (a1..a5 chained on the device)
  *
  * "Nemotron-Labs-TwoTower" wiki, "Block-wise generation": a block starts fully
