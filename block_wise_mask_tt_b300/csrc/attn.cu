@@ -5,21 +5,31 @@
 // context tower's layer-i KV cache followed by the denoiser's own layer-i keys and
 // values for the block, with bidirectional attention inside the block.
 //
-// Split pass, one CTA per (context split, 128-row tile, kv head, sequence):
-//   * rows of the tile are the packed (block position s, query head j of the GQA
-//     group) pairs, row = s*G + j, so one kv head's K/V tile serves G*S query rows
-//     and QK^T / PV are real dense contractions (M = 128, N = 64 keys, K = D);
-//   * Q (loaded once) and 64-token K/V tiles are staged in shared memory by TMA with
-//     128-byte swizzle; K/V use a 2-stage ring so the next tile streams in while the
-//     current one is processed;
-//   * S = Q K^T is accumulated in tensor memory (TMEM), read back one row per
-//     thread, turned into P = exp2(S*scale*log2e - m) with an online max that is
-//     only raised (and O rescaled in TMEM) when it grows by more than 2^8;
-//   * P (bf16) goes to shared memory in the canonical K-major swizzled layout and
-//     O += P V is accumulated in TMEM (V as an MN-major operand, no transpose);
-//   * the tile's (m, l, O) partial state goes to the workspace.
+// Split pass, one CTA per (context split, row group, kv head, sequence):
+//   * the rows are the packed (block position s, query head j of the GQA group)
+//     pairs, row = s*G + j.  One CTA serves up to 256 of them as one or two 128-row
+//     MMA tiles, so every K/V tile it loads feeds G*S query rows and QK^T / PV are
+//     dense contractions (M = 128, N = 128 keys, K = D for QK^T; N = D, K = 128 for PV);
+//   * warp 0 streams 128-token K/V tiles (two 64-row TMA boxes each, so a tile may
+//     span two pages of a paged cache) into a shared-memory ring with 128-byte
+//     swizzle; warp 1 issues every tcgen05.mma; warpgroup i (warps 4i+4 .. 4i+7) owns
+//     128-row tile i, one row per thread / TMEM lane;
+//   * Q sits in shared memory for the whole CTA; the scores S go to tensor memory
+//     (TMEM); the softmax warpgroup turns them into P = exp2(S*scale*log2e - m)
+//     (bf16) written back over the front of S, which is the TMEM A operand of PV; O
+//     accumulates in TMEM.  N = 128 keys per QK^T instruction keeps the tensor core
+//     near its peak rate (64-key products run at little more than half of it);
+//   * the two tiles ping-pong: the MMA warp issues QK(0,j) QK(1,j) | PV(0,j)
+//     QK(0,j+1) | PV(1,j) QK(1,j+1) | ..., so one warpgroup's softmax overlaps the
+//     other's matrix products;
+//   * the running max is raised (and O rescaled in TMEM) only when it grows by more
+//     than 2^8, so most tiles need no correction;
+//   * the partial state (m, l, O) of each row goes to the workspace.
 // Merge pass, one CTA per (block position, kv head, sequence), one warp per query
 // head: combines the partial states of the splits and the S block keys.
+//
+// Every wait is bounded: a wait that runs out sets the device error word, the CTA
+// drains what it issued and returns.
 #include <math_constants.h>
 
 #include "tt_device.cuh"
@@ -28,26 +38,37 @@
 namespace tti {
 namespace {
 
-constexpr int kSplitThreads = 128;
-constexpr int kTileKeys = 64;
+constexpr int kTileKeys = 128;  // context keys per pipeline round (two 64-token pages)
+constexpr int kSub = 64;        // keys per TMA box (one page of a paged cache)
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 2-3 spare, 4-11 softmax
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kPrefetchTiles = 4;          // tiles pulled into L2 beyond the smem ring
 
 template <int D>
-struct SplitSmem {
-    static constexpr int NP = D / 64;                    // 64-element (128 B) column parts
-    static constexpr uint32_t kQPart = 128 * 128;        // 128 rows x 128 B
-    static constexpr uint32_t kKVPart = kTileKeys * 128; // 64 rows x 128 B
-    static constexpr uint32_t kStage = NP * kKVPart;
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + NP * kQPart;
-    static constexpr uint32_t kV = kK + 2 * kStage;
-    static constexpr uint32_t kP = kV + 2 * kStage;
-    static constexpr uint32_t kBar = kP + 128 * 128;
-    static constexpr uint32_t kEnd = kBar + 64;
-    static constexpr uint32_t kBytes = kEnd + 1024;       // alignment slack
-    static constexpr uint32_t kTmemCols = (D == 128) ? 256 : 128;
-    static constexpr uint32_t kOCol = (D == 128) ? 128 : 64;
+struct Cfg {
+    static constexpr int NP = D / 64;                      // 128-byte column parts of a row
+    static constexpr uint32_t kPart = kTileKeys * 128;     // 128 rows x 128 B (one part of a tile)
+    static constexpr uint32_t kTile = NP * kPart;          // one K (or V) tile
+    static constexpr uint32_t kStage = 2 * kTile;          // K then V
+    static constexpr int kStages = (D == 128) ? 2 : 4;     // K/V ring depth (128 KiB)
+    static constexpr uint32_t kQPart = 128 * 128;          // 128 query rows x 128 B
+    static constexpr uint32_t kQTile = NP * kQPart;        // one 128-row Q tile
+    static constexpr uint32_t kRing = 2 * kQTile;          // Q tiles first, then the ring
+    static constexpr uint32_t kBar = kRing + kStages * kStage;
+    // mbarriers: full[st], empty[st], s_full[2], p_full[2], o_full, q_ready; then the
+    // TMEM slot
+    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
+    static constexpr uint32_t kEnd = kSlot + 16;
+    static constexpr uint32_t kBytes = kEnd + 1024;        // alignment slack
+    // TMEM columns (512 allocated): S_i at 128 i (P_i, bf16, over its first 64);
+    // O_i at 256 + D i.
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColO = 256;
+    static_assert(kColO + 2 * D <= 512, "TMEM budget");
+    static_assert(kBytes <= 227 * 1024, "shared memory budget");
+    static_assert(256 * (D * 4 + 16) <= kBar, "epilogue staging fits in the Q tiles + ring");
 };
 
 __device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
@@ -61,36 +82,34 @@ __device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kSplitThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ AttnSplitParams p,
-                      const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-    using L = SplitSmem<D>;
-    constexpr int NP = L::NP;
+    using C = Cfg<D>;
+    constexpr int NP = C::NP;
+    constexpr int NS = C::kStages;
     constexpr uint32_t kIdescQK = ttk::idesc_bf16(128, kTileKeys, false, false);
     constexpr uint32_t kIdescPV = ttk::idesc_bf16(128, D, false, true);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 48);
-    volatile int* sh_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 56);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kSlot);
 
     const AttnGeom& g = p.g;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int split = blockIdx.x;
-    const int gkv = blockIdx.y / g.n_row_tiles;
-    const int rt = blockIdx.y % g.n_row_tiles;
+    const int rg = blockIdx.x % g.n_rg;
+    const int split = blockIdx.x / g.n_rg;
+    const int gkv = blockIdx.y;
     const int b = blockIdx.z;
 
     if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return;
     const int cap = g.page_size ? g.max_pages * g.page_size : g.max_ctx;
     const int ctx = p.ctx_len ? __ldg(p.ctx_len + b) : g.max_ctx;
     if (ctx < 0 || ctx > cap) {
-        if (tid == 0 && split == 0 && blockIdx.y == 0) ttk::report_error(p.err, ttk::kErrDevice);
+        if (tid == 0 && split == 0 && rg == 0) ttk::report_error(p.err, ttk::kErrDevice);
         return;
     }
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
@@ -98,246 +117,362 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
     const int t1 = min(n_tiles, t0 + g.tiles_per_split);
     if (t0 >= t1) return;  // this split is empty; the merge pass does not read it
     const int nt = t1 - t0;
-
-    const int row_local = tid;  // TMEM lane == tile row == thread
-    const int r_global = rt * g.rows_per_tile + row_local;
-    const bool row_valid = row_local < g.rows_per_tile && r_global < g.R;
-    const size_t pidx =
-        ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + (size_t)r_global;
+    const int n_mt = g.n_mt;
 
     if (g.page_size) {
+        // Every page this split reads must exist; pages past the context end are not read.
+        const int pg0 = t0 * 2;
+        const int pg1 = min(t1 * 2, (ctx + kSub - 1) / kSub);
         int bad = 0;
-        for (int t = t0 + tid; t < t1; t += kSplitThreads) {
+        for (int t = pg0 + tid; t < pg1; t += kThreads) {
             const int pg = __ldg(p.page_table + (size_t)b * g.max_pages + t);
             bad |= (pg < 0 || pg >= g.num_pages) ? 1 : 0;
         }
         if (__syncthreads_or(bad)) {
+            // Leave an empty partial state for every row so the merge skips this split.
             if (tid == 0) ttk::report_error(p.err, ttk::kErrDevice);
-            if (row_valid) {
-                p.part_ml[2 * pidx + 0] = -CUDART_INF_F;
-                p.part_ml[2 * pidx + 1] = 0.f;
+            for (int r = tid; r < g.rows_per_cta; r += kThreads) {
+                const int rglob = rg * 256 + r;
+                if (rglob < g.R) {
+                    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + rglob;
+                    p.part_ml[2 * pi + 0] = -CUDART_INF_F;
+                    p.part_ml[2 * pi + 1] = 0.f;
+                }
             }
             return;
         }
     }
 
-    const uint32_t sQ = ttk::smem_u32(smem + L::kQ);
-    const uint32_t sK = ttk::smem_u32(smem + L::kK);
-    const uint32_t sV = ttk::smem_u32(smem + L::kV);
-    const uint32_t sP = ttk::smem_u32(smem + L::kP);
-    const uint32_t bar_q = ttk::smem_u32(&bars[0]);
-    const uint32_t bar_full0 = ttk::smem_u32(&bars[1]);
-    const uint32_t bar_mma = ttk::smem_u32(&bars[3]);
+    const uint32_t sQ = ttk::smem_u32(smem);
+    const uint32_t sRing = ttk::smem_u32(smem + C::kRing);
+    const uint32_t bar0 = ttk::smem_u32(smem + C::kBar);
+    auto full_bar = [&](int st) { return bar0 + 8u * (uint32_t)st; };
+    auto empty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(NS + st); };
+    auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * NS + i); };
+    auto pfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * NS + 2 + i); };
+    const uint32_t ofull_bar = bar0 + 8u * (uint32_t)(2 * NS + 4);
+    const uint32_t qready_bar = bar0 + 8u * (uint32_t)(2 * NS + 5);
 
-    if (warp == 0) {
-        ttk::tmem_alloc(ttk::smem_u32(tmem_slot), L::kTmemCols);
+    if (warp == 1) {
+        ttk::tmem_alloc(ttk::smem_u32(tmem_slot), 512);
         ttk::tmem_relinquish();
     }
     if (tid == 0) {
-        ttk::mbar_init(bar_q, 1);
-        ttk::mbar_init(bar_full0, 1);
-        ttk::mbar_init(bar_full0 + 8, 1);
-        ttk::mbar_init(bar_mma, 1);
+        for (int st = 0; st < NS; ++st) {
+            ttk::mbar_init(full_bar(st), 1);
+            ttk::mbar_init(empty_bar(st), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ttk::mbar_init(sfull_bar(i), 1);
+            ttk::mbar_init(pfull_bar(i), 128);
+        }
+        ttk::mbar_init(ofull_bar, 1);
+        ttk::mbar_init(qready_bar, 128 * n_mt);
         ttk::fence_mbar_init();
     }
-    // Rows past the packed (s, head) rows of this tile are zero so they stay finite.
-    if (row_local >= g.rows_per_tile) {
-#pragma unroll
-        for (int part = 0; part < NP; ++part) {
-            uint4* dst = reinterpret_cast<uint4*>(smem + L::kQ + part * L::kQPart + row_local * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-    ttk::fence_proxy_async_smem();
     ttk::tc_fence_before();
     __syncthreads();
     ttk::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem;
-    const uint32_t tO = tmem + L::kOCol;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-    auto kv_row = [&](int t) -> int {
-        if (g.page_size) return __ldg(p.page_table + (size_t)b * g.max_pages + t) * kTileKeys;
-        return b * g.max_ctx + t * kTileKeys;
-    };
-    auto issue_kv = [&](int stage, int t) {
-        const uint32_t fb = bar_full0 + 8u * (uint32_t)stage;
-        const int row0 = kv_row(t);
-        ttk::mbar_arrive_expect_tx(fb, 2u * L::kStage);
-#pragma unroll
-        for (int part = 0; part < NP; ++part) {
-            ttk::tma_load_3d(sK + stage * L::kStage + part * L::kKVPart, &tmk, part * 64, gkv, row0, fb);
-            ttk::tma_load_3d(sV + stage * L::kStage + part * L::kKVPart, &tmv, part * 64, gkv, row0, fb);
-        }
-    };
+    const int wg = warp / 4 - 1;           // softmax warpgroup 0/1, or -1 for warps 0-3
+    const int lane_row = tid & 127;        // TMEM lane (tile row) of this softmax thread
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int r_local = wg * 128 + lane_row;               // row within this CTA
+    const int r_glob = rg * 256 + r_local;                 // packed row of (b, gkv)
+    const bool in_tile = wg >= 0 && wg < n_mt;
+    const bool row_valid = in_tile && r_local < g.rows_per_cta && r_glob < g.R;
 
-    if (tid == 0) {
-        ttk::mbar_arrive_expect_tx(bar_q, (uint32_t)(NP * g.rows_per_tile * 128));
-#pragma unroll
-        for (int part = 0; part < NP; ++part)
-            ttk::tma_load_3d(sQ + part * L::kQPart, &tmq, part * 64, gkv * g.G,
-                             b * g.S + rt * g.s_per_tile, bar_q);
-        issue_kv(0, t0);
-    }
-
-    float m_run = -CUDART_INF_F;
-    float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-        const int stage = j & 1;
-        const int t = t0 + j;
-        // ---- S = Q K^T (one thread issues; everyone else waits at the CTA barrier)
-        if (tid == 0) {
-            if (j + 1 < nt) issue_kv(stage ^ 1, t + 1);
-            bool w = (j > 0) || ttk::mbar_wait(bar_q, 0);
-            w = w && ttk::mbar_wait(bar_full0 + 8u * (uint32_t)stage, (uint32_t)((j >> 1) & 1));
-            if (w) {
-                ttk::tc_fence_after();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if ((tid & 31) == 0) {
+            // First cache row of half h of context tile t.  A second half past the
+            // context end re-reads the first half's rows (they are masked out), so
+            // every box is in range and no page past the sequence is looked up.
+            auto tile_row = [&](int t, int h) -> int {
+                const int hh = (t * kTileKeys + h * kSub < ctx) ? h : 0;
+                return g.page_size ? __ldg(p.page_table + (size_t)b * g.max_pages + 2 * t + hh) * kSub
+                                   : b * g.max_ctx + t * kTileKeys + hh * kSub;
+            };
+            int pf = NS;  // next tile (relative to t0) to pull into L2
+            int issued = 0;
+            for (int j = 0; j < nt; ++j) {
+                // Keep kPrefetchTiles tiles beyond the ring on their way into L2, so the
+                // loads below find them there instead of paying the full DRAM latency.
+                for (; pf < nt && pf < j + NS + kPrefetchTiles; ++pf) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int row0 = tile_row(t0 + pf, h);
+#pragma unroll
+                        for (int part = 0; part < NP; ++part) {
+                            ttk::tma_prefetch_3d(&tmk, part * 64, gkv, row0);
+                            ttk::tma_prefetch_3d(&tmv, part * 64, gkv, row0);
+                        }
+                    }
+                }
+                const int st = j % NS;
+                if (j >= NS && !ttk::mbar_wait(empty_bar(st), (uint32_t)(((j / NS) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar(st);
+                ttk::mbar_arrive_expect_tx(fb, C::kStage);
+                const uint32_t dK = sRing + (uint32_t)st * C::kStage;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row0 = tile_row(t0 + j, h);
+#pragma unroll
+                    for (int part = 0; part < NP; ++part) {
+                        const uint32_t off = part * C::kPart + h * (kSub * 128);
+                        ttk::tma_load_3d(dK + off, &tmk, part * 64, gkv, row0, fb);
+                        ttk::tma_load_3d(dK + C::kTile + off, &tmv, part * 64, gkv, row0, fb);
+                    }
+                }
+                ++issued;
+            }
+            if (!ok) ttk::report_error(p.err, ttk::kErrTimeout);
+            // Drain: the most recent load of every stage must have landed before exit.
+            for (int st = 0; st < NS && st < issued; ++st) {
+                const int jl = st + ((issued - 1 - st) / NS) * NS;
+                ttk::mbar_wait(full_bar(st), (uint32_t)((jl / NS) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if ((tid & 31) == 0) {
+            auto qk = [&](int i, int j) {
+                const uint32_t sK = sRing + (uint32_t)(j % NS) * C::kStage;
+                const uint32_t sQi = sQ + (uint32_t)i * C::kQTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t koff = (uint32_t)(k & 3) * 32u;
-                    const uint64_t a = ttk::sdesc_sw128(sQ + (k >> 2) * L::kQPart + koff, 16, 1024);
-                    const uint64_t bd =
-                        ttk::sdesc_sw128(sK + stage * L::kStage + (k >> 2) * L::kKVPart + koff, 16, 1024);
-                    ttk::mma_bf16_ss(tS, a, bd, kIdescQK, k > 0 ? 1u : 0u);
+                    const uint32_t koff = (uint32_t)(k >> 2) * C::kPart + (k & 3) * 32;
+                    const uint64_t ad = ttk::sdesc_sw128(sQi + (uint32_t)(k >> 2) * C::kQPart + (k & 3) * 32, 16, 1024);
+                    const uint64_t bd = ttk::sdesc_sw128(sK + koff, 16, 1024);
+                    ttk::mma_bf16_ss(tmem + C::kColS + 128 * i, ad, bd, kIdescQK, k > 0 ? 1u : 0u);
                 }
-                ttk::mma_commit(bar_mma);
-                w = ttk::mbar_wait(bar_mma, 0);
-            }
-            *sh_flag = w ? 1 : 0;
-        }
-        __syncthreads();
-        if (*sh_flag == 0) {
-            ok = false;
-            break;
-        }
-        ttk::tc_fence_after();
-
-        // ---- softmax on this thread's row
-        uint32_t s0[32], s1[32];
-        ttk::tmem_ld32(tS + lane_off + 0, s0);
-        ttk::tmem_ld32(tS + lane_off + 32, s1);
-        ttk::tmem_ld_wait32(s0);
-        tie32(s1);
-        const int lim = ctx - t * kTileKeys;  // keys at or past lim are outside the context
-        float x[64];
-        float mx = -CUDART_INF_F;
+                ttk::mma_commit(sfull_bar(i));
+            };
+            auto pv = [&](int i, int j) {
+                const uint32_t sV = sRing + (uint32_t)(j % NS) * C::kStage + C::kTile;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]) * g.scale_log2;
-            x[c] = (c < lim) ? v : -CUDART_INF_F;
-            mx = fmaxf(mx, x[c]);
-        }
-        if (j == 0) {
-            m_run = mx;
-        } else {
-            const bool need = mx > m_run + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? exp2f(m_run - mx) : 1.0f;
-                if (need) {
-                    m_run = mx;
-                    l_run *= alpha;
+                for (int k = 0; k < kTileKeys / 16; ++k) {
+                    const uint64_t bd = ttk::sdesc_sw128(sV + k * 2048, C::kPart, 1024);
+                    ttk::mma_bf16_ts(tmem + C::kColO + i * D, tmem + C::kColS + 128 * i + 8 * k, bd,
+                                     kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
                 }
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t o[32];
-                    ttk::tmem_ld32(tO + lane_off + cc, o);
-                    ttk::tmem_ld_wait32(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    ttk::tmem_st32(tO + lane_off + cc, o);
+            };
+            auto wait_full = [&](int j) { return ttk::mbar_wait(full_bar(j % NS), (uint32_t)((j / NS) & 1)); };
+            ok = ttk::mbar_wait(qready_bar, 0) && wait_full(0);
+            if (ok) {
+                ttk::tc_fence_after();
+                qk(0, 0);
+                if (n_mt == 2) qk(1, 0);
+            }
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t par = (uint32_t)(j & 1);
+                if (!(ok = ttk::mbar_wait(pfull_bar(0), par))) break;
+                ttk::tc_fence_after();
+                pv(0, j);
+                const bool next = j + 1 < nt;
+                if (next) {
+                    if (!(ok = wait_full(j + 1))) break;
+                    ttk::tc_fence_after();
+                    qk(0, j + 1);
                 }
-                ttk::tmem_st_wait();
+                if (n_mt == 2) {
+                    if (!(ok = ttk::mbar_wait(pfull_bar(1), par))) break;
+                    ttk::tc_fence_after();
+                    pv(1, j);
+                }
+                ttk::mma_commit(empty_bar(j % NS));  // K/V of tile j are no longer read
+                if (next && n_mt == 2) qk(1, j + 1);
             }
+            if (!ok) ttk::report_error(p.err, ttk::kErrTimeout);
+            // Completion of everything issued: the epilogue waits for it, and so does
+            // this lane before the TMEM release below (also after a timeout).
+            ttk::mma_commit(ofull_bar);
+            ttk::mbar_wait(ofull_bar, 0);
         }
-        float lsum = 0.f;
-        uint8_t* prow = smem + L::kP + row_local * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p0 = exp2f(x[8 * c8 + 2 * e] - m_run);
-                const float p1 = exp2f(x[8 * c8 + 2 * e + 1] - m_run);
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
-                lsum += __low2float(pr) + __high2float(pr);
-                w4[e] = *reinterpret_cast<const uint32_t*>(&pr);
-            }
-            *reinterpret_cast<uint4*>(prow + ((c8 ^ (row_local & 7)) << 4)) =
-                make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        l_run += lsum;
-        if (lim < kTileKeys) {
-            // Last tile of a context that ends inside it: the V rows past the end are
-            // whatever the cache holds there (another sequence, an unused page slot).
-            // P is 0 for them, but 0 * NaN would still poison O, so zero those rows.
-            constexpr int kChunksPerRow = NP * 8;  // 16-byte chunks per V row
-            uint8_t* vst = smem + L::kV + stage * L::kStage;
-            for (int i = tid; i < (kTileKeys - lim) * kChunksPerRow; i += kSplitThreads) {
-                const int key = lim + i / kChunksPerRow;
-                const int ch = i % kChunksPerRow;
-                *reinterpret_cast<uint4*>(vst + (ch >> 3) * L::kKVPart + key * 128 + ((ch & 7) << 4)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        ttk::fence_proxy_async_smem();
-        ttk::tc_fence_before();
-        __syncthreads();
-
-        // ---- O += P V
-        if (tid == 0) {
-            ttk::tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < kTileKeys / 16; ++k) {
-                const uint64_t a = ttk::sdesc_sw128(sP + k * 32, 16, 1024);
-                const uint64_t bd = ttk::sdesc_sw128(sV + stage * L::kStage + k * 2048, L::kKVPart, 1024);
-                ttk::mma_bf16_ss(tO, a, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-            }
-            ttk::mma_commit(bar_mma);
-            *sh_flag = ttk::mbar_wait(bar_mma, 1) ? 1 : 0;
-        }
-        __syncthreads();
-        if (*sh_flag == 0) {
-            ok = false;
-            break;
-        }
-        ttk::tc_fence_after();
-    }
-
-    if (ok) {
-        // tcgen05.ld is warp-collective: every lane loads, only rows in range store.
-        float* acc = p.part_acc + pidx * D;
-#pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-            uint32_t o[32];
-            ttk::tmem_ld32(tO + lane_off + cc, o);
-            ttk::tmem_ld_wait32(o);
+    } else if (in_tile) {
+        // ---- this thread's Q row into shared memory (canonical K-major, 128-B swizzle)
+        {
+            uint4 qv[D / 8];
             if (row_valid) {
+                const int s = r_glob / g.G, j = r_glob % g.G;
+                const uint4* qp = reinterpret_cast<const uint4*>(
+                    p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(acc + cc + e) =
-                        make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                    __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+                for (int c = 0; c < D / 8; ++c) qv[c] = __ldg(qp + c);
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            uint8_t* qrow = smem + (size_t)wg * C::kQTile + (size_t)lane_row * 128;
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c)
+                *reinterpret_cast<uint4*>(qrow + (c >> 3) * C::kQPart + (((c & 7) ^ (lane_row & 7)) << 4)) = qv[c];
+            ttk::fence_proxy_async_smem();
+            ttk::mbar_arrive(qready_bar);
+        }
+        // ------------------------------------------------------------ softmax tile wg
+        const uint32_t tS = tmem + lane_off + C::kColS + 128 * wg;
+        const uint32_t tO = tmem + lane_off + C::kColO + wg * D;
+        const uint64_t scale2 = ttk::f2_pack(g.scale_log2, g.scale_log2);
+        float m_run = -CUDART_INF_F;
+        float l_run = 0.f;
+        for (int j = 0; j < nt; ++j) {
+            if (!ttk::mbar_wait(sfull_bar(wg), (uint32_t)(j & 1))) {
+                ok = false;
+                break;
+            }
+            ttk::tc_fence_after();
+            const int lim = ctx - (t0 + j) * kTileKeys;  // keys at or past lim lie outside
+            // pass 1: row max of the raw scores (scale > 0 commutes with the max)
+            float r0 = -CUDART_INF_F, r1 = -CUDART_INF_F;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a0[32], a1[32];
+                ttk::tmem_ld32(tS + 64 * h, a0);
+                ttk::tmem_ld32(tS + 64 * h + 32, a1);
+                ttk::tmem_ld_wait32(a0);
+                tie32(a1);
+                if (lim >= kTileKeys) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        r0 = ttk::fmax3(r0, __uint_as_float(a0[c]), __uint_as_float(a0[c + 1]));
+                        r1 = ttk::fmax3(r1, __uint_as_float(a1[c]), __uint_as_float(a1[c + 1]));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int k0 = 64 * h + c, k1 = 64 * h + 32 + c;
+                        r0 = fmaxf(r0, k0 < lim ? __uint_as_float(a0[c]) : -CUDART_INF_F);
+                        r1 = fmaxf(r1, k1 < lim ? __uint_as_float(a1[c]) : -CUDART_INF_F);
+                    }
+                }
+            }
+            const float mx = fmaxf(r0, r1) * g.scale_log2;
+            if (j == 0) {
+                m_run = mx;
+            } else {
+                const bool need = mx > m_run + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O_wg is stable here: PV(wg, j-1) completed before QK(wg, j).
+                    const float alpha = need ? exp2f(m_run - mx) : 1.0f;
+                    if (need) {
+                        m_run = mx;
+                        l_run *= alpha;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t o[32];
+                        ttk::tmem_ld32(tO + cc, o);
+                        ttk::tmem_ld_wait32(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        ttk::tmem_st32(tO + cc, o);
+                    }
+                }
+            }
+            // pass 2: p = 2^(s*scale*log2e - m) in chunks of 32 keys, one packed FMA per
+            // pair then the SFU; P (bf16 pairs) is written over the already-read front of
+            // S.  The row sum adds the bf16-rounded p that PV multiplies V by.
+            const uint64_t negm2 = ttk::f2_pack(-m_run, -m_run);
+            uint64_t lsum2 = ttk::f2_pack(0.f, 0.f);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t a[32];
+                ttk::tmem_ld32(tS + 32 * q4, a);
+                ttk::tmem_ld_wait32(a);
+                if (lim < kTileKeys) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (32 * q4 + c >= lim) a[c] = __float_as_uint(-CUDART_INF_F);
+                }
+                uint32_t pw[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    float e0, e1;
+                    ttk::f2_unpack(ttk::f2_fma(ttk::f2_pack(__uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1])),
+                                               scale2, negm2), e0, e1);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ttk::ex2_ftz(e0), ttk::ex2_ftz(e1));
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(&pr);
+                    pw[c] = w;
+                    lsum2 = ttk::f2_add(lsum2, ttk::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
+                }
+                ttk::tmem_st16(tS + 16 * q4, pw);
+            }
+            {
+                float a, bq;
+                ttk::f2_unpack(lsum2, a, bq);
+                l_run += a + bq;
+            }
+            if (wg == 0 && lim < kTileKeys) {
+                // Last tile of a context that ends inside it: the V rows past the end
+                // hold whatever the cache has there.  P is 0 for them, but 0 * NaN
+                // would still poison O, so zero those rows before PV(0, j) reads them
+                // (PV(1, j) is issued after PV(0, j)).  K and V of this tile have
+                // landed: QK(wg, j) has completed.
+                uint8_t* vst = smem + C::kRing + (size_t)(j % NS) * C::kStage + C::kTile;
+                constexpr int kChunks = NP * 8;  // 16-byte chunks per V row
+                for (int i2 = lane_row; i2 < (kTileKeys - lim) * kChunks; i2 += 128) {
+                    const int key = lim + i2 / kChunks;
+                    const int ch = i2 % kChunks;
+                    *reinterpret_cast<uint4*>(vst + (ch >> 3) * C::kPart + key * 128 + ((ch & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                ttk::fence_proxy_async_smem();
+            }
+            ttk::tmem_st_wait();
+            ttk::tc_fence_before();
+            ttk::mbar_arrive(pfull_bar(wg));
+        }
+        if (ok) ok = ttk::mbar_wait(ofull_bar, 0);
+        if (!ok) {
+            if (lane_row == 0) ttk::report_error(p.err, ttk::kErrTimeout);
+            if (row_valid) {
+                const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
+                p.part_ml[2 * pi + 0] = -CUDART_INF_F;
+                p.part_ml[2 * pi + 1] = 0.f;
+            }
+        } else {
+            // Epilogue: each O row goes TMEM -> registers -> shared memory (the Q tiles and
+            // the K/V ring are idle once every MMA has completed) -> one bulk copy of the
+            // row's contiguous D floats.  A row stride of D*4 + 16 bytes keeps the
+            // 16-byte stores of consecutive rows in different banks.
+            ttk::tc_fence_after();
+            constexpr uint32_t kRowStride = D * 4 + 16;
+            uint8_t* orow = smem + (size_t)r_local * kRowStride;
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t o[32];
+                ttk::tmem_ld32(tO + cc, o);  // warp-collective: every lane loads
+                ttk::tmem_ld_wait32(o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<uint4*>(orow + (cc + 4 * e) * 4) =
+                        make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+            }
+            if (row_valid) {
+                const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
+                ttk::fence_proxy_async_smem();
+                ttk::bulk_store(p.part_acc + pi * D, ttk::smem_u32(orow), D * 4);
+                ttk::bulk_commit();
+                p.part_ml[2 * pi + 0] = m_run;
+                p.part_ml[2 * pi + 1] = l_run;
+                ttk::bulk_wait_all();
             }
         }
-        if (row_valid) {
-            p.part_ml[2 * pidx + 0] = m_run;
-            p.part_ml[2 * pidx + 1] = l_run;
-        }
-    } else {
-        if (tid == 0) ttk::report_error(p.err, ttk::kErrTimeout);
-        if (row_valid) {
-            p.part_ml[2 * pidx + 0] = -CUDART_INF_F;
-            p.part_ml[2 * pidx + 1] = 0.f;
-        }
     }
+
+    // TMEM is released only after every MMA this CTA issued has completed (the
+    // issuing lane waited for that above).
     ttk::tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         ttk::tc_fence_after();
-        ttk::tmem_dealloc(tmem, L::kTmemCols);
+        ttk::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -345,8 +480,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
 // Merge: partial states of the context splits + the S block keys -> out, lse.
 // ---------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(512) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
-    constexpr int PER = D / 32;  // head dims per lane
+__global__ void __launch_bounds__(512, 1) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
+    constexpr int PER = D / 32;       // head dims per lane
+    constexpr int KW = D / 2 + 1;     // 32-bit words per staged block-key row (padded)
+    constexpr int kEarly = 8;         // split states whose accumulators are requested up front
+    constexpr int kMaxWarps = 16;
     const AttnGeom& g = p.g;
     const int s = blockIdx.x, gkv = blockIdx.y, b = blockIdx.z;
     if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return;
@@ -358,69 +496,109 @@ __global__ void __launch_bounds__(512) attn_merge_kernel(const __grid_constant__
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
     const int n_valid = (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split;
 
-    for (int j = warp; j < g.G; j += nwarps) {
+    // The block's own keys (padded rows, so lane k reads row k without bank conflicts)
+    // and values for this kv head, staged once for all G heads; one query row per warp.
+    __shared__ uint32_t sk[32 * KW];
+    __shared__ __align__(16) uint16_t sv[32 * D];
+    __shared__ uint32_t sq[kMaxWarps][D / 2];
+    for (int i = threadIdx.x; i < g.S * (D / 2); i += blockDim.x) {
+        const int k = i / (D / 2), c = i % (D / 2);
+        const size_t off = (((size_t)b * g.S + k) * g.Hkv + gkv) * D;
+        sk[k * KW + c] = __ldg(reinterpret_cast<const uint32_t*>(p.k_blk + off) + c);
+    }
+    for (int i = threadIdx.x; i < g.S * (D / 8); i += blockDim.x) {
+        const int k = i / (D / 8), c = i % (D / 8);
+        const size_t off = (((size_t)b * g.S + k) * g.Hkv + gkv) * D;
+        reinterpret_cast<uint4*>(sv)[i] = __ldg(reinterpret_cast<const uint4*>(p.v_blk + off) + c);
+    }
+
+    const int iters = (g.G + nwarps - 1) / nwarps;  // the same for every warp
+    for (int it = 0; it < iters; ++it) {
+        const int j = warp + it * nwarps;
+        const bool active = j < g.G;
         const int h = gkv * g.G + j;
         const int r = s * g.G + j;
-        // query row slice
-        float q[PER];
-        {
-            const uint16_t* qp = p.q + (((size_t)b * g.S + s) * g.Hq + h) * D + lane * PER;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) q[e] = ttk::bf16_bits_to_f32(qp[e]);
-        }
-        // block keys: lane k ends up holding the scaled logit of block key k
-        float xk = -CUDART_INF_F;
-        for (int k = 0; k < g.S; ++k) {
-            const uint16_t* kp = p.k_blk + (((size_t)b * g.S + k) * g.Hkv + gkv) * D + lane * PER;
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) d = fmaf(q[e], ttk::bf16_bits_to_f32(kp[e]), d);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == k) xk = d * g.scale_log2;
-        }
-        // split states: lanes read (m_c, l_c) for c = lane, lane + 32, ...
         const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + (size_t)r;
-        float mloc = xk;
-        for (int c = lane; c < n_valid; c += 32)
-            mloc = fmaxf(mloc, __ldcg(p.part_ml + 2 * (base + (size_t)c * g.R)));
-        float m = mloc;
+        // Everything that does not depend on the weights is requested first.
+        float mc0 = -CUDART_INF_F, lc0 = 0.f;
+        float a[kEarly][PER];
+#pragma unroll
+        for (int u = 0; u < kEarly; ++u)
+#pragma unroll
+            for (int e = 0; e < PER; ++e) a[u][e] = 0.f;
+        if (active) {
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q + (((size_t)b * g.S + s) * g.Hq + h) * D);
+            for (int c = lane; c < D / 2; c += 32) sq[warp][c] = __ldg(qw + c);
+            if (lane < n_valid) {
+                const size_t pi = base + (size_t)lane * g.R;
+                mc0 = __ldcg(p.part_ml + 2 * pi);
+                lc0 = __ldcg(p.part_ml + 2 * pi + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < kEarly; ++u) {
+                if (u < n_valid) {
+                    const float* ap = p.part_acc + (base + (size_t)u * g.R) * D + lane * PER;
+                    if (PER == 4) {
+                        const float4 a4 = __ldcg(reinterpret_cast<const float4*>(ap));
+                        a[u][0] = a4.x; a[u][1 % PER] = a4.y; a[u][2 % PER] = a4.z; a[u][3 % PER] = a4.w;
+                    } else {
+                        const float2 a2 = __ldcg(reinterpret_cast<const float2*>(ap));
+                        a[u][0] = a2.x; a[u][1 % PER] = a2.y;
+                    }
+                }
+            }
+        }
+        if (it == 0) __syncthreads();  // block keys and values are staged
+        else __syncwarp();             // this warp's query row is staged
+        if (!active) continue;
+        // Block-key logits: lane k < S computes q . k_blk[k] from the staged rows.
+        float xk = -CUDART_INF_F;
+        if (lane < g.S) {
+            float d0 = 0.f, d1 = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < D / 2; ++c) {
+                const uint32_t qv = sq[warp][c];
+                const uint32_t kv = sk[lane * KW + c];
+                d0 = fmaf(ttk::bf16_bits_to_f32(qv & 0xFFFFu), ttk::bf16_bits_to_f32(kv & 0xFFFFu), d0);
+                d1 = fmaf(ttk::bf16_bits_to_f32(qv >> 16), ttk::bf16_bits_to_f32(kv >> 16), d1);
+            }
+            xk = (d0 + d1) * g.scale_log2;
+        }
+        float m = fmaxf(xk, mc0);
+        for (int c = lane + 32; c < n_valid; c += 32)
+            m = fmaxf(m, __ldcg(p.part_ml + 2 * (base + (size_t)c * g.R)));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        // Weights.  An empty partial state (m = -inf, l = 0) gets weight 0 and is
+        // selected away rather than multiplied, since its accumulator was never written.
+        const float wk = (lane < g.S) ? exp2f(xk - m) : 0.f;
+        const float wc0 = (lane < n_valid && mc0 != -CUDART_INF_F) ? exp2f(mc0 - m) : 0.f;
+        float lloc = wk + wc0 * lc0;  // lanes >= 32 splits are added below
         float acc[PER];
 #pragma unroll
         for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-        float lloc = (lane < g.S) ? exp2f(xk - m) : 0.f;
-        const float wk = lloc;
-        for (int c0 = 0; c0 < n_valid; c0 += 32) {
-            const int c = c0 + lane;
-            float wc = 0.f;
-            if (c < n_valid) {
-                const size_t pi = base + (size_t)c * g.R;
+#pragma unroll
+        for (int u = 0; u < kEarly; ++u) {
+            const float w = __shfl_sync(0xffffffffu, wc0, u);
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = (w != 0.f) ? fmaf(w, a[u][e], acc[e]) : acc[e];
+        }
+        // Split states beyond the first kEarly (long contexts with many splits).
+        for (int cc = kEarly; cc < n_valid; ++cc) {
+            float w;
+            if (cc < 32) {
+                w = __shfl_sync(0xffffffffu, wc0, cc);
+            } else {
+                const size_t pi = base + (size_t)cc * g.R;
                 const float mc = __ldcg(p.part_ml + 2 * pi);
-                if (mc != -CUDART_INF_F) {
-                    wc = exp2f(mc - m);
-                    lloc = fmaf(wc, __ldcg(p.part_ml + 2 * pi + 1), lloc);
-                }
+                w = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - m);
+                if (lane == 0) lloc = fmaf(w, __ldcg(p.part_ml + 2 * pi + 1), lloc);
             }
-            const int nc = min(32, n_valid - c0);
-#pragma unroll 4
-            for (int cc = 0; cc < nc; ++cc) {
-                const float w = __shfl_sync(0xffffffffu, wc, cc);
-                if (w != 0.f) {
-                    const float* ap = p.part_acc + (base + (size_t)(c0 + cc) * g.R) * D + lane * PER;
-                    if (PER == 4) {
-                        const float4 a4 = __ldcg(reinterpret_cast<const float4*>(ap));
-                        acc[0] = fmaf(w, a4.x, acc[0]);
-                        acc[1] = fmaf(w, a4.y, acc[1]);
-                        acc[2 % PER] = fmaf(w, a4.z, acc[2 % PER]);
-                        acc[3 % PER] = fmaf(w, a4.w, acc[3 % PER]);
-                    } else {
-                        const float2 a2 = __ldcg(reinterpret_cast<const float2*>(ap));
-                        acc[0] = fmaf(w, a2.x, acc[0]);
-                        acc[1 % PER] = fmaf(w, a2.y, acc[1 % PER]);
-                    }
-                }
+            const float* ap = p.part_acc + (base + (size_t)cc * g.R) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) {
+                const float a1 = __ldcg(ap + e);
+                acc[e] = (w != 0.f) ? fmaf(w, a1, acc[e]) : acc[e];
             }
         }
         float l = lloc;
@@ -428,7 +606,7 @@ __global__ void __launch_bounds__(512) attn_merge_kernel(const __grid_constant__
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         for (int k = 0; k < g.S; ++k) {
             const float w = __shfl_sync(0xffffffffu, wk, k);
-            const uint16_t* vp = p.v_blk + (((size_t)b * g.S + k) * g.Hkv + gkv) * D + lane * PER;
+            const uint16_t* vp = sv + k * D + lane * PER;
 #pragma unroll
             for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, ttk::bf16_bits_to_f32(vp[e]), acc[e]);
         }
@@ -441,7 +619,19 @@ __global__ void __launch_bounds__(512) attn_merge_kernel(const __grid_constant__
         }
         if (p.lse != nullptr && lane == 0)
             p.lse[((size_t)b * g.S + s) * g.Hq + h] = (m + log2f(l)) * 0.6931471805599453f;
+        __syncwarp();  // sq[warp] is rewritten by the next iteration
     }
+}
+
+// Modelled cost, in quarter tile-times, of splitting every (sequence, kv head, row
+// group) item's n_tiles context tiles into `splits` ranges: waves of one CTA per SM,
+// each paying its tiles plus ~3 tiles of set-up, pipeline fill and epilogue; the merge's
+// serial depth (8 partial states in flight per round); and the partial-state traffic.
+long long split_cost(long long items, int n_tiles, int splits) {
+    const long long ctas = items * splits;
+    const long long waves = (ctas + 147) / 148;
+    const long long tps = (n_tiles + splits - 1) / splits;
+    return 4 * waves * (tps + 3) + 4 * ((splits + 7) / 8) + (2 * ctas) / 148;
 }
 
 }  // namespace
@@ -457,10 +647,11 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     if (S > 32) { *why = "S must be at most 32"; return false; }
     if (g.G > 128) { *why = "Hq/Hkv must be at most 128"; return false; }
     if (g.G * S > 512) { *why = "(Hq/Hkv)*S must be at most 512"; return false; }
-    g.s_per_tile = (128 / g.G < S) ? 128 / g.G : S;
-    g.rows_per_tile = g.s_per_tile * g.G;
-    g.n_row_tiles = (S + g.s_per_tile - 1) / g.s_per_tile;
+    if (Hkv > 65535 || B > 65535) { *why = "B and Hkv must be at most 65535"; return false; }
     g.R = g.G * S;
+    g.rows_per_cta = g.R < 256 ? g.R : 256;
+    g.n_rg = (g.R + 255) / 256;
+    g.n_mt = (g.rows_per_cta + 127) / 128;
     g.page_size = page_size;
     g.max_pages = max_pages;
     g.num_pages = num_pages;
@@ -478,21 +669,29 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     if (!(softmax_scale > 0.f) || !(softmax_scale < 1e30f)) { *why = "softmax_scale must be positive and finite"; return false; }
     g.scale_log2 = softmax_scale * kLog2e;
     const int n_tiles = (g.max_ctx + kTileKeys - 1) / kTileKeys;
-    const long long items = (long long)B * Hkv * g.n_row_tiles;
+    const long long items = (long long)B * Hkv * g.n_rg;
     int tps;
     if (num_splits > 0) {
         tps = n_tiles > 0 ? (n_tiles + num_splits - 1) / num_splits : 1;
+    } else if (n_tiles == 0) {
+        tps = 1;
     } else {
-        const long long target = 148LL * 2;
-        long long want = (target + items - 1) / items;
-        if (want < 1) want = 1;
-        tps = (int)((n_tiles + want - 1) / want);
-        if (tps > 64) tps = 64;
+        int best = 1;
+        long long best_cost = split_cost(items, n_tiles, 1);
+        const int max_s = n_tiles < 1024 ? n_tiles : 1024;
+        for (int s = 2; s <= max_s; ++s) {
+            const long long c = split_cost(items, n_tiles, s);
+            if (c < best_cost) { best_cost = c; best = s; }
+        }
+        tps = (n_tiles + best - 1) / best;
+        // A paged batch is ragged: shorter sequences leave their later splits empty
+        // (those CTAs exit at once), so keep splits long enough to amortise a CTA.
+        if (page_size != 0 && tps < 64 && n_tiles > 64) tps = 64;
     }
     if (tps < 1) tps = 1;
     g.tiles_per_split = tps;
     g.n_splits = n_tiles > 0 ? (n_tiles + tps - 1) / tps : 1;
-    if (g.n_splits > 65535) { *why = "too many context splits"; return false; }
+    if ((long long)g.n_splits * g.n_rg > (1LL << 30)) { *why = "too many context splits"; return false; }
     return true;
 }
 
@@ -512,21 +711,21 @@ cudaError_t attn_split_prepare(int D) {
     if (dev >= 0 && dev < 64 && ((done >> dev) & 1ull)) return cudaSuccess;
     if (D == 128)
         e = cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SplitSmem<128>::kBytes);
+                                 (int)Cfg<128>::kBytes);
     else
         e = cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SplitSmem<64>::kBytes);
+                                 (int)Cfg<64>::kBytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done |= (1ull << dev);
     return e;
 }
 
 cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cudaStream_t stream) {
     const AttnGeom& g = p.g;
-    dim3 grid(g.n_splits, g.Hkv * g.n_row_tiles, g.B);
+    dim3 grid(g.n_splits * g.n_rg, g.Hkv, g.B);
     if (g.D == 128)
-        attn_split_kernel<128><<<grid, kSplitThreads, SplitSmem<128>::kBytes, stream>>>(p, maps.q, maps.k, maps.v);
+        attn_split_kernel<128><<<grid, kThreads, Cfg<128>::kBytes, stream>>>(p, maps.k, maps.v);
     else
-        attn_split_kernel<64><<<grid, kSplitThreads, SplitSmem<64>::kBytes, stream>>>(p, maps.q, maps.k, maps.v);
+        attn_split_kernel<64><<<grid, kThreads, Cfg<64>::kBytes, stream>>>(p, maps.k, maps.v);
     return cudaGetLastError();
 }
 

@@ -157,7 +157,6 @@ tt_status plan_attn(const tt_attn_dims* d, const void* q, const void* k_blk, con
         TT_TRY(need_ptr(v_ctx, "v_ctx"));
         TT_TRY(encode_3d(&pl.maps.k, k_ctx, g.D, g.Hkv, rows, 1, 64));
         TT_TRY(encode_3d(&pl.maps.v, v_ctx, g.D, g.Hkv, rows, 1, 64));
-        TT_TRY(encode_3d(&pl.maps.q, q, g.D, g.Hq, (uint64_t)g.B * g.S, g.G, g.s_per_tile));
         TT_CUDA(tti::attn_split_prepare(g.D));
     }
     return TT_OK;
@@ -176,6 +175,7 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     if (pl.has_ctx) {
         tti::AttnSplitParams sp;
         sp.g = g;
+        sp.q = static_cast<const uint16_t*>(q);
         sp.ctx_len = ctx_len;
         sp.page_table = page_table;
         sp.skip_if_zero = skip_if_zero;

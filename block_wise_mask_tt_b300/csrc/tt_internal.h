@@ -77,10 +77,10 @@ cudaError_t unmask_noalloc_scratch(void** out);
 // -------------------------------------------------------------------------- attention
 struct AttnGeom {
     int B, S, Hq, Hkv, G, D;
-    int s_per_tile;    // block positions per 128-row tile
-    int rows_per_tile; // s_per_tile * G (<= 128)
-    int n_row_tiles;
-    int R;             // G * S rows per (sequence, kv head)
+    int R;             // G * S packed query rows per (sequence, kv head), row = s * G + j
+    int rows_per_cta;  // min(R, 256): rows one split CTA serves (one or two 128-row tiles)
+    int n_rg;          // row groups per (sequence, kv head): ceil(R / 256)
+    int n_mt;          // 128-row MMA tiles per CTA: ceil(rows_per_cta / 128)
     int max_ctx;       // contiguous: token stride; paged: max_pages * page_size
     int page_size;     // 0 or 64
     int max_pages, num_pages;
@@ -95,6 +95,7 @@ size_t attn_workspace_bytes(const AttnGeom& g);
 
 struct AttnSplitParams {
     AttnGeom g;
+    const uint16_t* q;           // bf16 [B][S][Hq][D]
     const int32_t* ctx_len;      // nullable (contiguous only)
     const int32_t* page_table;   // nullable
     const int32_t* skip_if_zero; // nullable
@@ -103,8 +104,7 @@ struct AttnSplitParams {
     int* err;
 };
 struct AttnMaps {
-    CUtensorMap q;   // bf16 [B*S][Hq][D], box (64, G, s_per_tile)
-    CUtensorMap k;   // bf16 [rows][Hkv][D], box (64, 1, 64)
+    CUtensorMap k;   // bf16 [rows][Hkv][D], box (64, 1, 64), 128-B swizzle
     CUtensorMap v;
 };
 cudaError_t attn_split_prepare(int D);  // sets the kernel's shared-memory limit on this device
