@@ -1,5 +1,5 @@
-// Denoise attention: split-KV pass over the context cache on tcgen05, then a merge
-// pass that also folds in the block's own (bidirectional) keys.
+// Denoise attention: split-KV pass over the context cache on tcgen05, then (when a
+// row's context is split) a pass that combines the partial states.
 //
 // "Nemotron-Labs-TwoTower" wiki, "Architecture": block queries attend over the
 // context tower's layer-i KV cache followed by the denoiser's own layer-i keys and
@@ -10,23 +10,28 @@
 //     pairs, row = s*G + j.  One CTA serves up to 256 of them as one or two 128-row
 //     MMA tiles, so every K/V tile it loads feeds G*S query rows and QK^T / PV are
 //     dense contractions (M = 128, N = 128 keys, K = D for QK^T; N = D, K = 128 for PV);
+//   * split 0 also takes the block's own S keys, as one extra (masked) key tile in
+//     front of its context tiles, so the block keys run on the tensor cores too;
 //   * warp 0 streams 128-token K/V tiles (two 64-row TMA boxes each, so a tile may
 //     span two pages of a paged cache) into a shared-memory ring with 128-byte
-//     swizzle; warp 1 issues every tcgen05.mma; warpgroup i (warps 4i+4 .. 4i+7) owns
-//     128-row tile i, one row per thread / TMEM lane;
+//     swizzle; warp 1 issues every tcgen05.mma; four softmax warpgroups own the rows:
+//     warpgroup (i, h) takes tile i's 128 rows (one per thread / TMEM lane) and keys
+//     64h .. 64h+63 of every 128-key tile.  The two halves of a row agree on its max
+//     through shared memory and a named barrier;
 //   * Q sits in shared memory for the whole CTA; the scores S go to tensor memory
-//     (TMEM); the softmax warpgroup turns them into P = exp2(S*scale*log2e - m)
-//     (bf16) written back over the front of S, which is the TMEM A operand of PV; O
-//     accumulates in TMEM.  N = 128 keys per QK^T instruction keeps the tensor core
-//     near its peak rate (64-key products run at little more than half of it);
-//   * the two tiles ping-pong: the MMA warp issues QK(0,j) QK(1,j) | PV(0,j)
-//     QK(0,j+1) | PV(1,j) QK(1,j+1) | ..., so one warpgroup's softmax overlaps the
-//     other's matrix products;
+//     (TMEM); the softmax turns them into P = exp2(S*scale*log2e - m) (bf16) written
+//     back over the front of each half's S columns, which is the TMEM A operand of
+//     PV; O accumulates in
+//     TMEM.  N = 128 keys per QK^T instruction keeps the tensor core near its peak
+//     rate (64-key products run at little more than half of it);
+//   * the two row tiles ping-pong: the MMA warp issues QK(0,j) QK(1,j) | PV(0,j)
+//     QK(0,j+1) | PV(1,j) QK(1,j+1) | ..., so one tile's softmax overlaps the other's
+//     matrix products;
 //   * the running max is raised (and O rescaled in TMEM) only when it grows by more
 //     than 2^8, so most tiles need no correction;
-//   * the partial state (m, l, O) of each row goes to the workspace.
-// Merge pass, one CTA per (block position, kv head, sequence), one warp per query
-// head: combines the partial states of the splits and the S block keys.
+//   * with a single split the CTA writes the normalised output (bf16) and the lse
+//     itself; otherwise each row's partial state (m, l, O) goes to the workspace and
+//     the combine pass (one warp per output row) merges them.
 //
 // Every wait is bounded: a wait that runs out sets the device error word, the CTA
 // drains what it issued and returns.
@@ -38,12 +43,12 @@
 namespace tti {
 namespace {
 
-constexpr int kTileKeys = 128;  // context keys per pipeline round (two 64-token pages)
+constexpr int kTileKeys = 128;  // keys per pipeline round (two 64-token pages)
 constexpr int kSub = 64;        // keys per TMA box (one page of a paged cache)
-constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 2-3 spare, 4-11 softmax
+constexpr int kThreads = 640;   // warp 0 TMA, warp 1 MMA, warps 2-3 spare, 4-19 softmax
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPrefetchTiles = 4;          // tiles pulled into L2 beyond the smem ring
 
 template <int D>
 struct Cfg {
@@ -55,7 +60,8 @@ struct Cfg {
     static constexpr uint32_t kQPart = 128 * 128;          // 128 query rows x 128 B
     static constexpr uint32_t kQTile = NP * kQPart;        // one 128-row Q tile
     static constexpr uint32_t kRing = 2 * kQTile;          // Q tiles first, then the ring
-    static constexpr uint32_t kBar = kRing + kStages * kStage;
+    static constexpr uint32_t kXchg = kRing + kStages * kStage;  // float [2 tiles][2 halves][128]
+    static constexpr uint32_t kBar = kXchg + 2 * 2 * 128 * 4;
     // mbarriers: full[st], empty[st], s_full[2], p_full[2], o_full, q_ready; then the
     // TMEM slot
     static constexpr int kNumBars = 2 * kStages + 6;
@@ -66,9 +72,12 @@ struct Cfg {
     // O_i at 256 + D i.
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColO = 256;
+    // Epilogue staging: one half row (D/2 floats) per softmax thread, padded so the
+    // 16-byte stores of consecutive rows fall in different banks.
+    static constexpr uint32_t kHalfRow = D * 2 + 16;
     static_assert(kColO + 2 * D <= 512, "TMEM budget");
     static_assert(kBytes <= 227 * 1024, "shared memory budget");
-    static_assert(256 * (D * 4 + 16) <= kBar, "epilogue staging fits in the Q tiles + ring");
+    static_assert(512 * kHalfRow <= kXchg, "epilogue staging fits in the Q tiles + ring");
 };
 
 __device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
@@ -81,11 +90,14 @@ __device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
                    "+r"(r[30]), "+r"(r[31]));
 }
 
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ AttnSplitParams p,
-                      const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv) {
+                      const __grid_constant__ AttnMaps maps) {
     using C = Cfg<D>;
     constexpr int NP = C::NP;
     constexpr int NS = C::kStages;
@@ -96,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kSlot);
+    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // [tile][half][row]
 
     const AttnGeom& g = p.g;
     const int tid = threadIdx.x;
@@ -112,14 +125,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && split == 0 && rg == 0) ttk::report_error(p.err, ttk::kErrDevice);
         return;
     }
+    // Tiles of this CTA: split 0 starts with the block's own keys, then context tiles
+    // t0 .. t1-1.
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
     const int t0 = split * g.tiles_per_split;
     const int t1 = min(n_tiles, t0 + g.tiles_per_split);
-    if (t0 >= t1) return;  // this split is empty; the merge pass does not read it
-    const int nt = t1 - t0;
+    const int nblk = (split == 0) ? 1 : 0;
+    const int nt = nblk + max(0, t1 - t0);
+    if (nt == 0) return;  // this split is empty; the combine pass does not read it
     const int n_mt = g.n_mt;
+    const bool direct = g.n_splits == 1;
 
-    if (g.page_size) {
+    if (g.page_size && t1 > t0) {
         // Every page this split reads must exist; pages past the context end are not read.
         const int pg0 = t0 * 2;
         const int pg1 = min(t1 * 2, (ctx + kSub - 1) / kSub);
@@ -129,14 +146,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bad |= (pg < 0 || pg >= g.num_pages) ? 1 : 0;
         }
         if (__syncthreads_or(bad)) {
-            // Leave an empty partial state for every row so the merge skips this split.
+            // Leave an empty partial state for every row so the combine skips this
+            // split (a single-split call has no partials: its output is left unwritten).
             if (tid == 0) ttk::report_error(p.err, ttk::kErrDevice);
-            for (int r = tid; r < g.rows_per_cta; r += kThreads) {
-                const int rglob = rg * 256 + r;
-                if (rglob < g.R) {
-                    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + rglob;
-                    p.part_ml[2 * pi + 0] = -CUDART_INF_F;
-                    p.part_ml[2 * pi + 1] = 0.f;
+            if (!direct) {
+                for (int r = tid; r < g.rows_per_cta; r += kThreads) {
+                    const int rglob = rg * 256 + r;
+                    if (rglob < g.R) {
+                        const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + rglob;
+                        p.part_ml[2 * pi + 0] = -CUDART_INF_F;
+                        p.part_ml[2 * pi + 1] = 0.f;
+                    }
                 }
             }
             return;
@@ -164,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ttk::mbar_init(sfull_bar(i), 1);
-            ttk::mbar_init(pfull_bar(i), 128);
+            ttk::mbar_init(pfull_bar(i), 256);
         }
         ttk::mbar_init(ofull_bar, 1);
         ttk::mbar_init(qready_bar, 128 * n_mt);
@@ -175,42 +195,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     ttk::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int wg = warp / 4 - 1;           // softmax warpgroup 0/1, or -1 for warps 0-3
+    const int q = warp / 4 - 1;            // softmax warpgroup 0..3, or -1 for warps 0-3
+    const int mt = q >> 1;                 // its 128-row tile
+    const int half = q & 1;                // its 64 keys of every 128-key tile
     const int lane_row = tid & 127;        // TMEM lane (tile row) of this softmax thread
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int r_local = wg * 128 + lane_row;               // row within this CTA
+    const int r_local = mt * 128 + lane_row;               // row within this CTA
     const int r_glob = rg * 256 + r_local;                 // packed row of (b, gkv)
-    const bool in_tile = wg >= 0 && wg < n_mt;
+    const bool in_tile = q >= 0 && mt < n_mt;
     const bool row_valid = in_tile && r_local < g.rows_per_cta && r_glob < g.R;
 
     bool ok = true;
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if ((tid & 31) == 0) {
-            // First cache row of half h of context tile t.  A second half past the
-            // context end re-reads the first half's rows (they are masked out), so
-            // every box is in range and no page past the sequence is looked up.
-            auto tile_row = [&](int t, int h) -> int {
-                const int hh = (t * kTileKeys + h * kSub < ctx) ? h : 0;
-                return g.page_size ? __ldg(p.page_table + (size_t)b * g.max_pages + 2 * t + hh) * kSub
-                                   : b * g.max_ctx + t * kTileKeys + hh * kSub;
-            };
-            int pf = NS;  // next tile (relative to t0) to pull into L2
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
-                // Keep kPrefetchTiles tiles beyond the ring on their way into L2, so the
-                // loads below find them there instead of paying the full DRAM latency.
-                for (; pf < nt && pf < j + NS + kPrefetchTiles; ++pf) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int row0 = tile_row(t0 + pf, h);
-#pragma unroll
-                        for (int part = 0; part < NP; ++part) {
-                            ttk::tma_prefetch_3d(&tmk, part * 64, gkv, row0);
-                            ttk::tma_prefetch_3d(&tmv, part * 64, gkv, row0);
-                        }
-                    }
-                }
                 const int st = j % NS;
                 if (j >= NS && !ttk::mbar_wait(empty_bar(st), (uint32_t)(((j / NS) - 1) & 1))) {
                     ok = false;
@@ -219,14 +219,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = full_bar(st);
                 ttk::mbar_arrive_expect_tx(fb, C::kStage);
                 const uint32_t dK = sRing + (uint32_t)st * C::kStage;
+                const bool blk = j < nblk;
+                const CUtensorMap* mk = blk ? &maps.kb : &maps.k;
+                const CUtensorMap* mv = blk ? &maps.vb : &maps.v;
+                const int t = t0 + j - nblk;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int row0 = tile_row(t0 + j, h);
+                    // A second half past the end (the block's S <= 32 keys, or the
+                    // context end) re-reads the first half's rows: they are masked
+                    // out, every box stays in range, and no page past the sequence is
+                    // looked up.
+                    int row0;
+                    if (blk) {
+                        row0 = b * g.S;
+                    } else {
+                        const int hh = (t * kTileKeys + h * kSub < ctx) ? h : 0;
+                        row0 = g.page_size ? __ldg(p.page_table + (size_t)b * g.max_pages + 2 * t + hh) * kSub
+                                           : b * g.max_ctx + t * kTileKeys + hh * kSub;
+                    }
 #pragma unroll
                     for (int part = 0; part < NP; ++part) {
                         const uint32_t off = part * C::kPart + h * (kSub * 128);
-                        ttk::tma_load_3d(dK + off, &tmk, part * 64, gkv, row0, fb);
-                        ttk::tma_load_3d(dK + C::kTile + off, &tmv, part * 64, gkv, row0, fb);
+                        ttk::tma_load_3d(dK + off, mk, part * 64, gkv, row0, fb);
+                        ttk::tma_load_3d(dK + C::kTile + off, mv, part * 64, gkv, row0, fb);
                     }
                 }
                 ++issued;
@@ -258,8 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     const uint64_t bd = ttk::sdesc_sw128(sV + k * 2048, C::kPart, 1024);
-                    ttk::mma_bf16_ts(tmem + C::kColO + i * D, tmem + C::kColS + 128 * i + 8 * k, bd,
-                                     kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+                    // keys 16k .. 16k+15: P of key half k/4 sits over the front of that
+                    // half's own 64 S columns
+                    const uint32_t pcol = C::kColS + 128 * i + 64 * (k >> 2) + 8 * (k & 3);
+                    ttk::mma_bf16_ts(tmem + C::kColO + i * D, tmem + pcol, bd, kIdescPV,
+                                     (j > 0 || k > 0) ? 1u : 0u);
                 }
             };
             auto wait_full = [&](int j) { return ttk::mbar_wait(full_bar(j % NS), (uint32_t)((j / NS) & 1)); };
@@ -295,48 +313,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             ttk::mbar_wait(ofull_bar, 0);
         }
     } else if (in_tile) {
-        // ---- this thread's Q row into shared memory (canonical K-major, 128-B swizzle)
-        {
-            uint4 qv[D / 8];
-            if (row_valid) {
-                const int s = r_glob / g.G, j = r_glob % g.G;
-                const uint4* qp = reinterpret_cast<const uint4*>(
-                    p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D);
+        // ---- this row's Q into shared memory (canonical K-major, 128-B swizzle)
+        if (half == 0) {
+            const int s = r_glob / g.G, j = r_glob % g.G;
+            const uint4* qp = reinterpret_cast<const uint4*>(
+                p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D);
+            uint8_t* qrow = smem + (size_t)mt * C::kQTile + (size_t)lane_row * 128;
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) qv[c] = __ldg(qp + c);
-            } else {
+            for (int part = 0; part < NP; ++part) {  // 128 bytes of the row at a time
+                uint4 qv[8];
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < 8; ++c) qv[c] = row_valid ? __ldg(qp + part * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(qrow + part * C::kQPart + ((c ^ (lane_row & 7)) << 4)) = qv[c];
             }
-            uint8_t* qrow = smem + (size_t)wg * C::kQTile + (size_t)lane_row * 128;
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c)
-                *reinterpret_cast<uint4*>(qrow + (c >> 3) * C::kQPart + (((c & 7) ^ (lane_row & 7)) << 4)) = qv[c];
             ttk::fence_proxy_async_smem();
             ttk::mbar_arrive(qready_bar);
         }
-        // ------------------------------------------------------------ softmax tile wg
-        const uint32_t tS = tmem + lane_off + C::kColS + 128 * wg;
-        const uint32_t tO = tmem + lane_off + C::kColO + wg * D;
+        // ------------------------------------------------- softmax: tile mt, keys half
+        const uint32_t tS = tmem + lane_off + C::kColS + 128 * mt;
+        const uint32_t tO = tmem + lane_off + C::kColO + mt * D;
         const uint64_t scale2 = ttk::f2_pack(g.scale_log2, g.scale_log2);
+        float* my_x = xchg + (mt * 2 + half) * 128 + lane_row;
+        const float* other_x = xchg + (mt * 2 + (half ^ 1)) * 128 + lane_row;
+        const int bar_id = 1 + mt;  // named barrier of this tile's two halves
         float m_run = -CUDART_INF_F;
-        float l_run = 0.f;
+        float l_part = 0.f;  // sum of p over this half's keys
         for (int j = 0; j < nt; ++j) {
-            if (!ttk::mbar_wait(sfull_bar(wg), (uint32_t)(j & 1))) {
+            if (!ttk::mbar_wait(sfull_bar(mt), (uint32_t)(j & 1))) {
                 ok = false;
                 break;
             }
             ttk::tc_fence_after();
-            const int lim = ctx - (t0 + j) * kTileKeys;  // keys at or past lim lie outside
-            // pass 1: row max of the raw scores (scale > 0 commutes with the max)
-            float r0 = -CUDART_INF_F, r1 = -CUDART_INF_F;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            const int lim = (j < nblk) ? g.S : ctx - (t0 + j - nblk) * kTileKeys;  // keys >= lim lie outside
+            const int k0 = 64 * half;  // first key of this half
+            float rmax = -CUDART_INF_F;
+            {
                 uint32_t a0[32], a1[32];
-                ttk::tmem_ld32(tS + 64 * h, a0);
-                ttk::tmem_ld32(tS + 64 * h + 32, a1);
+                ttk::tmem_ld32(tS + k0, a0);
+                ttk::tmem_ld32(tS + k0 + 32, a1);
                 ttk::tmem_ld_wait32(a0);
                 tie32(a1);
+                float r0 = -CUDART_INF_F, r1 = -CUDART_INF_F;
                 if (lim >= kTileKeys) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
@@ -346,74 +365,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const int k0 = 64 * h + c, k1 = 64 * h + 32 + c;
-                        r0 = fmaxf(r0, k0 < lim ? __uint_as_float(a0[c]) : -CUDART_INF_F);
-                        r1 = fmaxf(r1, k1 < lim ? __uint_as_float(a1[c]) : -CUDART_INF_F);
+                        r0 = fmaxf(r0, (k0 + c < lim) ? __uint_as_float(a0[c]) : -CUDART_INF_F);
+                        r1 = fmaxf(r1, (k0 + 32 + c < lim) ? __uint_as_float(a1[c]) : -CUDART_INF_F);
                     }
                 }
+                rmax = fmaxf(r0, r1);
             }
-            const float mx = fmaxf(r0, r1) * g.scale_log2;
+            // Row max of the raw scores over both halves (scale > 0 commutes with it).
+            *my_x = rmax;
+            ttk::tc_fence_before();
+            named_sync(bar_id, 256);
+            ttk::tc_fence_after();
+            const float mx = fmaxf(*my_x, *other_x) * g.scale_log2;
             if (j == 0) {
                 m_run = mx;
             } else {
                 const bool need = mx > m_run + kRescaleThreshold;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O_wg is stable here: PV(wg, j-1) completed before QK(wg, j).
+                    // O is stable here: PV(mt, j-1) completed before QK(mt, j).  Each
+                    // half rescales its D/2 columns of the row.
                     const float alpha = need ? exp2f(m_run - mx) : 1.0f;
                     if (need) {
                         m_run = mx;
-                        l_run *= alpha;
+                        l_part *= alpha;
                     }
 #pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
+                    for (int cc = 0; cc < D / 2; cc += 32) {
                         uint32_t o[32];
-                        ttk::tmem_ld32(tO + cc, o);
+                        ttk::tmem_ld32(tO + half * (D / 2) + cc, o);
                         ttk::tmem_ld_wait32(o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        ttk::tmem_st32(tO + cc, o);
+                        ttk::tmem_st32(tO + half * (D / 2) + cc, o);
                     }
                 }
             }
-            // pass 2: p = 2^(s*scale*log2e - m) in chunks of 32 keys, one packed FMA per
-            // pair then the SFU; P (bf16 pairs) is written over the already-read front of
-            // S.  The row sum adds the bf16-rounded p that PV multiplies V by.
+            // p = 2^(s*scale*log2e - m), 32 keys at a time re-read from TMEM: one packed
+            // FMA per pair, then the SFU.  P (bf16 pairs) goes over the front of this
+            // half's own 64 S columns, which only this thread reads.  The row sum adds
+            // the unrounded p.
             const uint64_t negm2 = ttk::f2_pack(-m_run, -m_run);
             uint64_t lsum2 = ttk::f2_pack(0.f, 0.f);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t a[32];
-                ttk::tmem_ld32(tS + 32 * q4, a);
+                ttk::tmem_ld32(tS + k0 + 32 * c2, a);
                 ttk::tmem_ld_wait32(a);
                 if (lim < kTileKeys) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        if (32 * q4 + c >= lim) a[c] = __float_as_uint(-CUDART_INF_F);
+                        if (k0 + 32 * c2 + c >= lim) a[c] = __float_as_uint(-CUDART_INF_F);
                 }
                 uint32_t pw[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
+                    const uint64_t e2 = ttk::f2_fma(ttk::f2_pack(__uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1])),
+                                                    scale2, negm2);
                     float e0, e1;
-                    ttk::f2_unpack(ttk::f2_fma(ttk::f2_pack(__uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1])),
-                                               scale2, negm2), e0, e1);
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ttk::ex2_ftz(e0), ttk::ex2_ftz(e1));
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(&pr);
-                    pw[c] = w;
-                    lsum2 = ttk::f2_add(lsum2, ttk::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
+                    ttk::f2_unpack(e2, e0, e1);
+                    const float p0 = ttk::ex2_ftz(e0), p1 = ttk::ex2_ftz(e1);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
+                    pw[c] = *reinterpret_cast<const uint32_t*>(&pr);
+                    lsum2 = ttk::f2_add(lsum2, ttk::f2_pack(p0, p1));
                 }
-                ttk::tmem_st16(tS + 16 * q4, pw);
+                ttk::tmem_st16(tS + k0 + 16 * c2, pw);
             }
             {
-                float a, bq;
-                ttk::f2_unpack(lsum2, a, bq);
-                l_run += a + bq;
+                float x0, x1;
+                ttk::f2_unpack(lsum2, x0, x1);
+                l_part += x0 + x1;
             }
-            if (wg == 0 && lim < kTileKeys) {
-                // Last tile of a context that ends inside it: the V rows past the end
+            if (q == 0 && lim < kTileKeys) {
+                // Last tile of a key range that ends inside it: the V rows past the end
                 // hold whatever the cache has there.  P is 0 for them, but 0 * NaN
                 // would still poison O, so zero those rows before PV(0, j) reads them
                 // (PV(1, j) is issued after PV(0, j)).  K and V of this tile have
-                // landed: QK(wg, j) has completed.
+                // landed: QK(0, j) has completed.
                 uint8_t* vst = smem + C::kRing + (size_t)(j % NS) * C::kStage + C::kTile;
                 constexpr int kChunks = NP * 8;  // 16-byte chunks per V row
                 for (int i2 = lane_row; i2 < (kTileKeys - lim) * kChunks; i2 += 128) {
@@ -426,41 +453,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ttk::tmem_st_wait();
             ttk::tc_fence_before();
-            ttk::mbar_arrive(pfull_bar(wg));
+            ttk::mbar_arrive(pfull_bar(mt));
         }
         if (ok) ok = ttk::mbar_wait(ofull_bar, 0);
+        // The row's l: this half's sum plus the other half's (same m for both).
+        float* my_l = xchg + (mt * 2 + half) * 128 + lane_row;
+        const float* other_l = xchg + (mt * 2 + (half ^ 1)) * 128 + lane_row;
+        named_sync(bar_id, 256);  // every read of the max slots is done
+        *my_l = ok ? l_part : 0.f;
+        named_sync(bar_id, 256);
+        const float l = l_part + *other_l;
         if (!ok) {
-            if (lane_row == 0) ttk::report_error(p.err, ttk::kErrTimeout);
-            if (row_valid) {
+            if (lane_row == 0 && half == 0) ttk::report_error(p.err, ttk::kErrTimeout);
+            if (row_valid && half == 0 && !direct) {
                 const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
                 p.part_ml[2 * pi + 0] = -CUDART_INF_F;
                 p.part_ml[2 * pi + 1] = 0.f;
             }
         } else {
-            // Epilogue: each O row goes TMEM -> registers -> shared memory (the Q tiles and
-            // the K/V ring are idle once every MMA has completed) -> one bulk copy of the
-            // row's contiguous D floats.  A row stride of D*4 + 16 bytes keeps the
-            // 16-byte stores of consecutive rows in different banks.
+            // Epilogue: this half's D/2 columns of the O row go TMEM -> registers ->
+            // shared memory (the Q tiles and the K/V ring are idle once every MMA has
+            // completed) -> one bulk copy.  Single split: normalised bf16 output;
+            // otherwise the fp32 partial accumulator.
             ttk::tc_fence_after();
-            constexpr uint32_t kRowStride = D * 4 + 16;
-            uint8_t* orow = smem + (size_t)r_local * kRowStride;
+            uint8_t* hrow = smem + (size_t)(r_local * 2 + half) * C::kHalfRow;
+            const float inv = 1.0f / l;
 #pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
+            for (int cc = 0; cc < D / 2; cc += 32) {
                 uint32_t o[32];
-                ttk::tmem_ld32(tO + cc, o);  // warp-collective: every lane loads
+                ttk::tmem_ld32(tO + half * (D / 2) + cc, o);  // warp-collective: every lane loads
                 ttk::tmem_ld_wait32(o);
+                if (direct) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<uint4*>(orow + (cc + 4 * e) * 4) =
-                        make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                                __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
+                            w[u] = *reinterpret_cast<const uint32_t*>(&pr);
+                        }
+                        *reinterpret_cast<uint4*>(hrow + (cc + 8 * e) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        *reinterpret_cast<uint4*>(hrow + (cc + 4 * e) * 4) =
+                            make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                }
             }
             if (row_valid) {
-                const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
                 ttk::fence_proxy_async_smem();
-                ttk::bulk_store(p.part_acc + pi * D, ttk::smem_u32(orow), D * 4);
-                ttk::bulk_commit();
-                p.part_ml[2 * pi + 0] = m_run;
-                p.part_ml[2 * pi + 1] = l_run;
+                if (direct) {
+                    const int s = r_glob / g.G, jh = r_glob % g.G;
+                    const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh;
+                    ttk::bulk_store(p.out + orow * D + half * (D / 2), ttk::smem_u32(hrow), D);
+                    ttk::bulk_commit();
+                    if (half == 0 && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
+                } else {
+                    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
+                    ttk::bulk_store(p.part_acc + pi * D + half * (D / 2), ttk::smem_u32(hrow), D * 2);
+                    ttk::bulk_commit();
+                    if (half == 0) {
+                        p.part_ml[2 * pi + 0] = m_run;
+                        p.part_ml[2 * pi + 1] = l;
+                    }
+                }
                 ttk::bulk_wait_all();
             }
         }
@@ -477,150 +535,86 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------
-// Merge: partial states of the context splits + the S block keys -> out, lse.
+// Combine: partial states of the context splits -> out, lse.  One warp per output
+// row (b, s, h); lanes hold D/32 columns each.
 // ---------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(512, 1) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
-    constexpr int PER = D / 32;       // head dims per lane
-    constexpr int KW = D / 2 + 1;     // 32-bit words per staged block-key row (padded)
-    constexpr int kEarly = 8;         // split states whose accumulators are requested up front
-    constexpr int kMaxWarps = 16;
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
+    constexpr int PER = D / 32;
+    constexpr int kBatch = 8;  // accumulators requested together
     const AttnGeom& g = p.g;
-    const int s = blockIdx.x, gkv = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= (long long)g.B * g.S * g.Hq) return;
+    const int h = (int)(row % g.Hq);
+    const int s = (int)((row / g.Hq) % g.S);
+    const int b = (int)(row / ((long long)g.Hq * g.S));
     if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
+    const int gkv = h / g.G, j = h % g.G;
     const int cap = g.page_size ? g.max_pages * g.page_size : g.max_ctx;
     int ctx = p.ctx_len ? __ldg(p.ctx_len + b) : g.max_ctx;
     if (ctx < 0 || ctx > cap) ctx = 0;  // reported by the split pass
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
-    const int n_valid = (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split;
+    // Split 0 always holds the block's keys; the others hold context tiles.
+    const int n_valid = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
+    const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + (size_t)(s * g.G + j);
 
-    // The block's own keys (padded rows, so lane k reads row k without bank conflicts)
-    // and values for this kv head, staged once for all G heads; one query row per warp.
-    __shared__ uint32_t sk[32 * KW];
-    __shared__ __align__(16) uint16_t sv[32 * D];
-    __shared__ uint32_t sq[kMaxWarps][D / 2];
-    for (int i = threadIdx.x; i < g.S * (D / 2); i += blockDim.x) {
-        const int k = i / (D / 2), c = i % (D / 2);
-        const size_t off = (((size_t)b * g.S + k) * g.Hkv + gkv) * D;
-        sk[k * KW + c] = __ldg(reinterpret_cast<const uint32_t*>(p.k_blk + off) + c);
-    }
-    for (int i = threadIdx.x; i < g.S * (D / 8); i += blockDim.x) {
-        const int k = i / (D / 8), c = i % (D / 8);
-        const size_t off = (((size_t)b * g.S + k) * g.Hkv + gkv) * D;
-        reinterpret_cast<uint4*>(sv)[i] = __ldg(reinterpret_cast<const uint4*>(p.v_blk + off) + c);
-    }
-
-    const int iters = (g.G + nwarps - 1) / nwarps;  // the same for every warp
-    for (int it = 0; it < iters; ++it) {
-        const int j = warp + it * nwarps;
-        const bool active = j < g.G;
-        const int h = gkv * g.G + j;
-        const int r = s * g.G + j;
-        const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + (size_t)r;
-        // Everything that does not depend on the weights is requested first.
-        float mc0 = -CUDART_INF_F, lc0 = 0.f;
-        float a[kEarly][PER];
+    float m = -CUDART_INF_F;
+    for (int c = lane; c < n_valid; c += 32) m = fmaxf(m, __ldcg(p.part_ml + 2 * (base + (size_t)c * g.R)));
 #pragma unroll
-        for (int u = 0; u < kEarly; ++u)
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float acc[PER];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) a[u][e] = 0.f;
-        if (active) {
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q + (((size_t)b * g.S + s) * g.Hq + h) * D);
-            for (int c = lane; c < D / 2; c += 32) sq[warp][c] = __ldg(qw + c);
-            if (lane < n_valid) {
-                const size_t pi = base + (size_t)lane * g.R;
-                mc0 = __ldcg(p.part_ml + 2 * pi);
-                lc0 = __ldcg(p.part_ml + 2 * pi + 1);
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float lsum = 0.f;
+    for (int c0 = 0; c0 < n_valid; c0 += 32) {
+        // lane c - c0 holds split c's weight; an empty partial state (m = -inf) gets
+        // weight 0 and is selected away, since its accumulator was never written.
+        const int c = c0 + lane;
+        float wc = 0.f;
+        if (c < n_valid) {
+            const size_t pi = base + (size_t)c * g.R;
+            const float mc = __ldcg(p.part_ml + 2 * pi);
+            if (mc != -CUDART_INF_F) {
+                wc = exp2f(mc - m);
+                lsum = fmaf(wc, __ldcg(p.part_ml + 2 * pi + 1), lsum);
             }
+        }
+        const int nc = min(32, n_valid - c0);
+        for (int cb = 0; cb < nc; cb += kBatch) {
+            float a[kBatch][PER];
 #pragma unroll
-            for (int u = 0; u < kEarly; ++u) {
-                if (u < n_valid) {
-                    const float* ap = p.part_acc + (base + (size_t)u * g.R) * D + lane * PER;
-                    if (PER == 4) {
-                        const float4 a4 = __ldcg(reinterpret_cast<const float4*>(ap));
-                        a[u][0] = a4.x; a[u][1 % PER] = a4.y; a[u][2 % PER] = a4.z; a[u][3 % PER] = a4.w;
-                    } else {
-                        const float2 a2 = __ldcg(reinterpret_cast<const float2*>(ap));
-                        a[u][0] = a2.x; a[u][1 % PER] = a2.y;
-                    }
+            for (int u = 0; u < kBatch; ++u) {
+                const int cu = min(cb + u, nc - 1);  // in range; duplicates get weight 0 below
+                const float* ap = p.part_acc + (base + (size_t)(c0 + cu) * g.R) * D + lane * PER;
+                if (PER == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(ap));
+                    a[u][0] = v.x; a[u][1 % PER] = v.y; a[u][2 % PER] = v.z; a[u][3 % PER] = v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(ap));
+                    a[u][0] = v.x; a[u][1 % PER] = v.y;
                 }
             }
-        }
-        if (it == 0) __syncthreads();  // block keys and values are staged
-        else __syncwarp();             // this warp's query row is staged
-        if (!active) continue;
-        // Block-key logits: lane k < S computes q . k_blk[k] from the staged rows.
-        float xk = -CUDART_INF_F;
-        if (lane < g.S) {
-            float d0 = 0.f, d1 = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < D / 2; ++c) {
-                const uint32_t qv = sq[warp][c];
-                const uint32_t kv = sk[lane * KW + c];
-                d0 = fmaf(ttk::bf16_bits_to_f32(qv & 0xFFFFu), ttk::bf16_bits_to_f32(kv & 0xFFFFu), d0);
-                d1 = fmaf(ttk::bf16_bits_to_f32(qv >> 16), ttk::bf16_bits_to_f32(kv >> 16), d1);
-            }
-            xk = (d0 + d1) * g.scale_log2;
-        }
-        float m = fmaxf(xk, mc0);
-        for (int c = lane + 32; c < n_valid; c += 32)
-            m = fmaxf(m, __ldcg(p.part_ml + 2 * (base + (size_t)c * g.R)));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        // Weights.  An empty partial state (m = -inf, l = 0) gets weight 0 and is
-        // selected away rather than multiplied, since its accumulator was never written.
-        const float wk = (lane < g.S) ? exp2f(xk - m) : 0.f;
-        const float wc0 = (lane < n_valid && mc0 != -CUDART_INF_F) ? exp2f(mc0 - m) : 0.f;
-        float lloc = wk + wc0 * lc0;  // lanes >= 32 splits are added below
-        float acc[PER];
+            for (int u = 0; u < kBatch; ++u) {
+                float w = __shfl_sync(0xffffffffu, wc, min(cb + u, 31));
+                if (cb + u >= nc) w = 0.f;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int u = 0; u < kEarly; ++u) {
-            const float w = __shfl_sync(0xffffffffu, wc0, u);
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = (w != 0.f) ? fmaf(w, a[u][e], acc[e]) : acc[e];
-        }
-        // Split states beyond the first kEarly (long contexts with many splits).
-        for (int cc = kEarly; cc < n_valid; ++cc) {
-            float w;
-            if (cc < 32) {
-                w = __shfl_sync(0xffffffffu, wc0, cc);
-            } else {
-                const size_t pi = base + (size_t)cc * g.R;
-                const float mc = __ldcg(p.part_ml + 2 * pi);
-                w = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - m);
-                if (lane == 0) lloc = fmaf(w, __ldcg(p.part_ml + 2 * pi + 1), lloc);
-            }
-            const float* ap = p.part_acc + (base + (size_t)cc * g.R) * D + lane * PER;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) {
-                const float a1 = __ldcg(ap + e);
-                acc[e] = (w != 0.f) ? fmaf(w, a1, acc[e]) : acc[e];
+                for (int e = 0; e < PER; ++e) acc[e] = (w != 0.f) ? fmaf(w, a[u][e], acc[e]) : acc[e];
             }
         }
-        float l = lloc;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        for (int k = 0; k < g.S; ++k) {
-            const float w = __shfl_sync(0xffffffffu, wk, k);
-            const uint16_t* vp = sv + k * D + lane * PER;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, ttk::bf16_bits_to_f32(vp[e]), acc[e]);
-        }
-        const float inv = 1.0f / l;
-        uint16_t* op = p.out + (((size_t)b * g.S + s) * g.Hq + h) * D + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; e += 2) {
-            const __nv_bfloat162 pr = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-            *reinterpret_cast<uint32_t*>(op + e) = *reinterpret_cast<const uint32_t*>(&pr);
-        }
-        if (p.lse != nullptr && lane == 0)
-            p.lse[((size_t)b * g.S + s) * g.Hq + h] = (m + log2f(l)) * 0.6931471805599453f;
-        __syncwarp();  // sq[warp] is rewritten by the next iteration
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = 1.0f / lsum;
+    const size_t orow = ((size_t)b * g.S + s) * g.Hq + h;
+    uint16_t* op = p.out + orow * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2) {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+        *reinterpret_cast<uint32_t*>(op + e) = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    if (p.lse != nullptr && lane == 0) p.lse[orow] = (m + log2f(lsum)) * kLn2;
 }
 
 // Modelled cost, in quarter tile-times, of splitting every (sequence, kv head, row
@@ -723,20 +717,21 @@ cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cu
     const AttnGeom& g = p.g;
     dim3 grid(g.n_splits * g.n_rg, g.Hkv, g.B);
     if (g.D == 128)
-        attn_split_kernel<128><<<grid, kThreads, Cfg<128>::kBytes, stream>>>(p, maps.k, maps.v);
+        attn_split_kernel<128><<<grid, kThreads, Cfg<128>::kBytes, stream>>>(p, maps);
     else
-        attn_split_kernel<64><<<grid, kThreads, Cfg<64>::kBytes, stream>>>(p, maps.k, maps.v);
+        attn_split_kernel<64><<<grid, kThreads, Cfg<64>::kBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream) {
     const AttnGeom& g = p.g;
-    dim3 grid(g.S, g.Hkv, g.B);
-    const int warps = g.G < 16 ? g.G : 16;
+    const long long rows = (long long)g.B * g.S * g.Hq;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (g.D == 128)
-        attn_merge_kernel<128><<<grid, warps * 32, 0, stream>>>(p);
+        attn_merge_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(p);
     else
-        attn_merge_kernel<64><<<grid, warps * 32, 0, stream>>>(p);
+        attn_merge_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

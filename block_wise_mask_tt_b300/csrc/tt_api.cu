@@ -152,13 +152,20 @@ tt_status plan_attn(const tt_attn_dims* d, const void* q, const void* k_blk, con
     }
     const uint64_t rows = g.page_size ? (uint64_t)g.num_pages * 64u : (uint64_t)g.B * g.max_ctx;
     pl.has_ctx = rows > 0;
+    TT_TRY(encode_3d(&pl.maps.kb, k_blk, g.D, g.Hkv, (uint64_t)g.B * g.S, 1, 64));
+    TT_TRY(encode_3d(&pl.maps.vb, v_blk, g.D, g.Hkv, (uint64_t)g.B * g.S, 1, 64));
     if (pl.has_ctx) {
         TT_TRY(need_ptr(k_ctx, "k_ctx"));
         TT_TRY(need_ptr(v_ctx, "v_ctx"));
         TT_TRY(encode_3d(&pl.maps.k, k_ctx, g.D, g.Hkv, rows, 1, 64));
         TT_TRY(encode_3d(&pl.maps.v, v_ctx, g.D, g.Hkv, rows, 1, 64));
-        TT_CUDA(tti::attn_split_prepare(g.D));
+    } else {
+        // No context: the kernel reads only the block's own keys; the context maps are
+        // never used, so they are given the block maps.
+        pl.maps.k = pl.maps.kb;
+        pl.maps.v = pl.maps.vb;
     }
+    TT_CUDA(tti::attn_split_prepare(g.D));
     return TT_OK;
 }
 
@@ -166,41 +173,42 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
                            const int32_t* page_table, const int32_t* ctx_len,
                            const int32_t* skip_if_zero, void* out, float* lse, void* ws,
                            int* err, cudaStream_t st) {
-    const tti::AttnGeom& g = pl.g;
+    (void)k_blk;
+    (void)v_blk;
+    tti::AttnGeom g = pl.g;
+    if (!pl.has_ctx) {
+        g.max_ctx = 0;
+        g.page_size = 0;
+    }
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc_bytes = rows * g.D * sizeof(float);
     acc_bytes = (acc_bytes + 255) & ~size_t(255);
     float* part_acc = static_cast<float*>(ws);
     float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-    if (pl.has_ctx) {
-        tti::AttnSplitParams sp;
-        sp.g = g;
-        sp.q = static_cast<const uint16_t*>(q);
-        sp.ctx_len = ctx_len;
-        sp.page_table = page_table;
-        sp.skip_if_zero = skip_if_zero;
-        sp.part_acc = part_acc;
-        sp.part_ml = part_ml;
-        sp.err = err;
-        TT_CUDA(tti::launch_attn_split(sp, pl.maps, st));
+    tti::AttnSplitParams sp;
+    sp.g = g;
+    sp.q = static_cast<const uint16_t*>(q);
+    sp.ctx_len = pl.has_ctx ? ctx_len : nullptr;
+    sp.page_table = pl.has_ctx ? page_table : nullptr;
+    sp.skip_if_zero = skip_if_zero;
+    sp.part_acc = part_acc;
+    sp.part_ml = part_ml;
+    sp.out = static_cast<uint16_t*>(out);
+    sp.lse = lse;
+    sp.err = err;
+    TT_CUDA(tti::launch_attn_split(sp, pl.maps, st));
+    if (g.n_splits > 1) {
+        tti::AttnMergeParams mp;
+        mp.g = g;
+        mp.ctx_len = sp.ctx_len;
+        mp.skip_if_zero = skip_if_zero;
+        mp.part_acc = part_acc;
+        mp.part_ml = part_ml;
+        mp.out = static_cast<uint16_t*>(out);
+        mp.lse = lse;
+        mp.err = err;
+        TT_CUDA(tti::launch_attn_merge(mp, st));
     }
-    tti::AttnMergeParams mp;
-    mp.g = g;
-    if (!pl.has_ctx) {
-        mp.g.max_ctx = 0;
-        mp.g.page_size = 0;
-    }
-    mp.q = static_cast<const uint16_t*>(q);
-    mp.k_blk = static_cast<const uint16_t*>(k_blk);
-    mp.v_blk = static_cast<const uint16_t*>(v_blk);
-    mp.ctx_len = pl.has_ctx ? ctx_len : nullptr;
-    mp.skip_if_zero = skip_if_zero;
-    mp.part_acc = part_acc;
-    mp.part_ml = part_ml;
-    mp.out = static_cast<uint16_t*>(out);
-    mp.lse = lse;
-    mp.err = err;
-    TT_CUDA(tti::launch_attn_merge(mp, st));
     return TT_OK;
 }
 

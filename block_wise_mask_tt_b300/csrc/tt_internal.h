@@ -101,20 +101,21 @@ struct AttnSplitParams {
     const int32_t* skip_if_zero; // nullable
     float* part_acc;             // [B][Hkv][n_splits][R][D]
     float* part_ml;              // [B][Hkv][n_splits][R][2]
+    uint16_t* out;               // bf16 [B][S][Hq][D]: written here when n_splits == 1
+    float* lse;                  // nullable, [B][S][Hq]: likewise
     int* err;
 };
 struct AttnMaps {
-    CUtensorMap k;   // bf16 [rows][Hkv][D], box (64, 1, 64), 128-B swizzle
-    CUtensorMap v;
+    CUtensorMap k;   // context keys, bf16 [rows][Hkv][D], box (64, 1, 64), 128-B swizzle
+    CUtensorMap v;   // context values
+    CUtensorMap kb;  // the block's own keys, bf16 [B*S][Hkv][D], same box
+    CUtensorMap vb;  // the block's own values
 };
 cudaError_t attn_split_prepare(int D);  // sets the kernel's shared-memory limit on this device
 cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cudaStream_t stream);
 
 struct AttnMergeParams {
     AttnGeom g;
-    const uint16_t* q;
-    const uint16_t* k_blk;
-    const uint16_t* v_blk;
     const int32_t* ctx_len;
     const int32_t* skip_if_zero;
     const float* part_acc;
