@@ -62,9 +62,10 @@ struct Cfg {
     static constexpr uint32_t kRing = 2 * kQTile;          // Q tiles first, then the ring
     static constexpr uint32_t kXchg = kRing + kStages * kStage;  // float [2 tiles][2 halves][128]
     static constexpr uint32_t kBar = kXchg + 2 * 2 * 128 * 4;
-    // mbarriers: full[st], empty[st], s_full[2], p_full[2], o_full, q_ready; then the
-    // TMEM slot
-    static constexpr int kNumBars = 2 * kStages + 6;
+    // mbarriers: k_full[st], v_full[st], k_empty[st], v_empty[st], s_full[2], p_full[2],
+    // o_full, q_ready; then the TMEM slot.  K and V of a stage are tracked apart: K is
+    // free again once both QK^T products have read it, a round before V.
+    static constexpr int kNumBars = 4 * kStages + 6;
     static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
     static constexpr uint32_t kEnd = kSlot + 16;
     static constexpr uint32_t kBytes = kEnd + 1024;        // alignment slack
@@ -166,12 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = ttk::smem_u32(smem);
     const uint32_t sRing = ttk::smem_u32(smem + C::kRing);
     const uint32_t bar0 = ttk::smem_u32(smem + C::kBar);
-    auto full_bar = [&](int st) { return bar0 + 8u * (uint32_t)st; };
-    auto empty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(NS + st); };
-    auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * NS + i); };
-    auto pfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * NS + 2 + i); };
-    const uint32_t ofull_bar = bar0 + 8u * (uint32_t)(2 * NS + 4);
-    const uint32_t qready_bar = bar0 + 8u * (uint32_t)(2 * NS + 5);
+    auto kfull_bar = [&](int st) { return bar0 + 8u * (uint32_t)st; };
+    auto vfull_bar = [&](int st) { return bar0 + 8u * (uint32_t)(NS + st); };
+    auto kempty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(2 * NS + st); };
+    auto vempty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(3 * NS + st); };
+    auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(4 * NS + i); };
+    auto pfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(4 * NS + 2 + i); };
+    const uint32_t ofull_bar = bar0 + 8u * (uint32_t)(4 * NS + 4);
+    const uint32_t qready_bar = bar0 + 8u * (uint32_t)(4 * NS + 5);
 
     if (warp == 1) {
         ttk::tmem_alloc(ttk::smem_u32(tmem_slot), 512);
@@ -179,8 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         for (int st = 0; st < NS; ++st) {
-            ttk::mbar_init(full_bar(st), 1);
-            ttk::mbar_init(empty_bar(st), 1);
+            ttk::mbar_init(kfull_bar(st), 1);
+            ttk::mbar_init(vfull_bar(st), 1);
+            ttk::mbar_init(kempty_bar(st), 1);
+            ttk::mbar_init(vempty_bar(st), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ttk::mbar_init(sfull_bar(i), 1);
@@ -209,49 +214,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if ((tid & 31) == 0) {
-            int issued = 0;
-            for (int j = 0; j < nt; ++j) {
+            int issued[2] = {0, 0};  // K and V tiles whose loads were issued
+            for (int j = 0; j < nt && ok; ++j) {
                 const int st = j % NS;
-                if (j >= NS && !ttk::mbar_wait(empty_bar(st), (uint32_t)(((j / NS) - 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = full_bar(st);
-                ttk::mbar_arrive_expect_tx(fb, C::kStage);
+                const uint32_t par = (uint32_t)(((j / NS) - 1) & 1);
                 const uint32_t dK = sRing + (uint32_t)st * C::kStage;
                 const bool blk = j < nblk;
-                const CUtensorMap* mk = blk ? &maps.kb : &maps.k;
-                const CUtensorMap* mv = blk ? &maps.vb : &maps.v;
                 const int t = t0 + j - nblk;
+                // First cache row of each 64-row half.  A second half past the end (the
+                // block's S <= 32 keys, or the context end) re-reads the first half's
+                // rows: they are masked out, every box stays in range, and no page past
+                // the sequence is looked up.
+                int row0[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    // A second half past the end (the block's S <= 32 keys, or the
-                    // context end) re-reads the first half's rows: they are masked
-                    // out, every box stays in range, and no page past the sequence is
-                    // looked up.
-                    int row0;
                     if (blk) {
-                        row0 = b * g.S;
+                        row0[h] = b * g.S;
                     } else {
                         const int hh = (t * kTileKeys + h * kSub < ctx) ? h : 0;
-                        row0 = g.page_size ? __ldg(p.page_table + (size_t)b * g.max_pages + 2 * t + hh) * kSub
-                                           : b * g.max_ctx + t * kTileKeys + hh * kSub;
-                    }
-#pragma unroll
-                    for (int part = 0; part < NP; ++part) {
-                        const uint32_t off = part * C::kPart + h * (kSub * 128);
-                        ttk::tma_load_3d(dK + off, mk, part * 64, gkv, row0, fb);
-                        ttk::tma_load_3d(dK + C::kTile + off, mv, part * 64, gkv, row0, fb);
+                        row0[h] = g.page_size ? __ldg(p.page_table + (size_t)b * g.max_pages + 2 * t + hh) * kSub
+                                              : b * g.max_ctx + t * kTileKeys + hh * kSub;
                     }
                 }
-                ++issued;
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {  // K, then V
+                    if (j >= NS && !ttk::mbar_wait(kv ? vempty_bar(st) : kempty_bar(st), par)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = kv ? vfull_bar(st) : kfull_bar(st);
+                    const CUtensorMap* map = kv ? (blk ? &maps.vb : &maps.v) : (blk ? &maps.kb : &maps.k);
+                    ttk::mbar_arrive_expect_tx(fb, C::kTile);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int part = 0; part < NP; ++part)
+                            ttk::tma_load_3d(dK + kv * C::kTile + part * C::kPart + h * (kSub * 128), map,
+                                             part * 64, gkv, row0[h], fb);
+                    issued[kv] = j + 1;
+                }
             }
             if (!ok) ttk::report_error(p.err, ttk::kErrTimeout);
-            // Drain: the most recent load of every stage must have landed before exit.
-            for (int st = 0; st < NS && st < issued; ++st) {
-                const int jl = st + ((issued - 1 - st) / NS) * NS;
-                ttk::mbar_wait(full_bar(st), (uint32_t)((jl / NS) & 1));
-            }
+            // Drain: the most recent loads of every stage must have landed before exit.
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv)
+                for (int st = 0; st < NS && st < issued[kv]; ++st) {
+                    const int jl = st + ((issued[kv] - 1 - st) / NS) * NS;
+                    ttk::mbar_wait(kv ? vfull_bar(st) : kfull_bar(st), (uint32_t)((jl / NS) & 1));
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -280,31 +290,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      (j > 0 || k > 0) ? 1u : 0u);
                 }
             };
-            auto wait_full = [&](int j) { return ttk::mbar_wait(full_bar(j % NS), (uint32_t)((j / NS) & 1)); };
-            ok = ttk::mbar_wait(qready_bar, 0) && wait_full(0);
+            auto wait_k = [&](int j) { return ttk::mbar_wait(kfull_bar(j % NS), (uint32_t)((j / NS) & 1)); };
+            auto wait_v = [&](int j) { return ttk::mbar_wait(vfull_bar(j % NS), (uint32_t)((j / NS) & 1)); };
+            ok = ttk::mbar_wait(qready_bar, 0) && wait_k(0);
             if (ok) {
                 ttk::tc_fence_after();
                 qk(0, 0);
                 if (n_mt == 2) qk(1, 0);
+                ttk::mma_commit(kempty_bar(0));  // K of tile 0 is no longer read
             }
             for (int j = 0; j < nt && ok; ++j) {
                 const uint32_t par = (uint32_t)(j & 1);
-                if (!(ok = ttk::mbar_wait(pfull_bar(0), par))) break;
+                if (!(ok = ttk::mbar_wait(pfull_bar(0), par) && wait_v(j))) break;
                 ttk::tc_fence_after();
                 pv(0, j);
                 const bool next = j + 1 < nt;
                 if (next) {
-                    if (!(ok = wait_full(j + 1))) break;
+                    if (!(ok = wait_k(j + 1))) break;
                     ttk::tc_fence_after();
                     qk(0, j + 1);
+                    if (n_mt == 1) ttk::mma_commit(kempty_bar((j + 1) % NS));
                 }
                 if (n_mt == 2) {
                     if (!(ok = ttk::mbar_wait(pfull_bar(1), par))) break;
                     ttk::tc_fence_after();
                     pv(1, j);
                 }
-                ttk::mma_commit(empty_bar(j % NS));  // K/V of tile j are no longer read
-                if (next && n_mt == 2) qk(1, j + 1);
+                ttk::mma_commit(vempty_bar(j % NS));  // V of tile j is no longer read
+                if (next && n_mt == 2) {
+                    qk(1, j + 1);
+                    ttk::mma_commit(kempty_bar((j + 1) % NS));
+                }
             }
             if (!ok) ttk::report_error(p.err, ttk::kErrTimeout);
             // Completion of everything issued: the epilogue waits for it, and so does
