@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ttk::mbar_init(pfull_bar(i), 256);
         }
         ttk::mbar_init(ofull_bar, 1);
-        ttk::mbar_init(qready_bar, 128 * n_mt);
+        ttk::mbar_init(qready_bar, 128 * n_mt * NP);
         ttk::fence_mbar_init();
     }
     ttk::tc_fence_before();
@@ -214,6 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if ((tid & 31) == 0) {
+            ttk::prefetch_tensormap(&maps.k);
+            ttk::prefetch_tensormap(&maps.v);
+            if (nblk) {
+                ttk::prefetch_tensormap(&maps.kb);
+                ttk::prefetch_tensormap(&maps.vb);
+            }
             int issued[2] = {0, 0};  // K and V tiles whose loads were issued
             for (int j = 0; j < nt && ok; ++j) {
                 const int st = j % NS;
@@ -330,20 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (in_tile) {
         // ---- this row's Q into shared memory (canonical K-major, 128-B swizzle)
-        if (half == 0) {
+        // Half h loads 128-byte part h of the row (D = 128: both halves, one part
+        // each, so the whole row arrives in one round trip; D = 64: half 0 alone).
+        if (half < NP) {
             const int s = r_glob / g.G, j = r_glob % g.G;
             const uint4* qp = reinterpret_cast<const uint4*>(
-                p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D);
-            uint8_t* qrow = smem + (size_t)mt * C::kQTile + (size_t)lane_row * 128;
+                p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D) + half * 8;
+            uint8_t* qrow = smem + (size_t)mt * C::kQTile + (size_t)half * C::kQPart + (size_t)lane_row * 128;
+            uint4 qv[8];
 #pragma unroll
-            for (int part = 0; part < NP; ++part) {  // 128 bytes of the row at a time
-                uint4 qv[8];
+            for (int c = 0; c < 8; ++c) qv[c] = row_valid ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) qv[c] = row_valid ? __ldg(qp + part * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(qrow + part * C::kQPart + ((c ^ (lane_row & 7)) << 4)) = qv[c];
-            }
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (lane_row & 7)) << 4)) = qv[c];
             ttk::fence_proxy_async_smem();
             ttk::mbar_arrive(qready_bar);
         }
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.part_ml[2 * pi + 1] = l;
                     }
                 }
-                ttk::bulk_wait_all();
+                ttk::bulk_wait_read();  // shared memory may be released; the writes land on their own
             }
         }
     }

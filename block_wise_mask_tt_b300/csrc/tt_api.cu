@@ -644,7 +644,7 @@ tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids, int32_
     tti::unmask_layout(B, S, V, scratch, p);
     p.err = err;
     // The array keeps whatever the previous call left; the tickets must start at zero.
-    TT_CUDA(cudaMemsetAsync(p.ticket, 0, (size_t)(B + 1) * sizeof(unsigned int), st));
+    TT_CUDA(cudaMemsetAsync(p.ticket, 0, (size_t)p.ticket_words * sizeof(unsigned int), st));
     TT_CUDA(tti::launch_unmask(p, st));
     return TT_OK;
 }

@@ -61,8 +61,10 @@ struct UnmaskParams {
     int max_steps;
     int chunk;      // vocabulary entries per CTA (multiple of 1024)
     int n_chunks;
-    UnmaskPartial* part;     // [B][S][n_chunks]
-    unsigned int* ticket;    // [B], zero on entry, zero on exit
+    UnmaskPartial* part;     // [B*S][n_chunks]: one per (row, vocabulary chunk)
+    UnmaskPartial* row_res;  // [B*S]: the row's merged (max, sum, argmax)
+    unsigned int* ticket;    // [B*S] row tickets then [B] sequence tickets: zero on entry, zero on exit
+    int ticket_words;        // B*S + B
     int* err;
 };
 size_t unmask_workspace_bytes(int B, int S, int V);

@@ -6,11 +6,14 @@
 // decoded positions stay fixed.
 //
 // Pass structure: a grid of (vocabulary chunk, position, sequence) CTAs streams the
-// fp32 logits of masked rows once (128-bit loads that bypass L1 and are marked
-// evict-first in L2), reducing each chunk to (max, lowest argmax, sum of exp).  The
-// last CTA of a sequence to finish (atomic ticket after a release fence; nothing
-// spins) merges the chunk partials of its S rows and applies the commit/remask
-// update in place with one warp.
+// fp32 logits of masked rows once (16-byte loads that bypass L1, four per thread per
+// batch, up to four batches per CTA with six CTAs resident per SM), reducing each chunk
+// to (max, lowest argmax, sum of exp).  Completion is
+// counted in two levels, so no ticket sees more than max(chunks per row, S) atomic
+// increments: the last chunk CTA of a row (atomic ticket after a release fence;
+// nothing spins) merges that row's chunk partials into a row result, and the last
+// row of a sequence to finish takes the commit/remask decision for its S <= 32
+// positions with one warp and applies it in place.
 #include <math_constants.h>
 
 #include <mutex>
@@ -22,6 +25,7 @@ namespace tti {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kBatch = 4;  // 16-byte loads per thread per batch
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Red {
@@ -83,42 +87,26 @@ __device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&
     acc.s += s;
 }
 
-// Runs on the whole CTA that finished sequence b last.  Every warp merges the chunk
-// partials of some rows (lanes over chunks, so the loads are independent), then warp
-// 0 takes the commit/remask decision for the S <= 32 positions.
-__device__ void decide(const UnmaskParams& p, int b, float* sh_conf, int* sh_tok, int* sh_masked) {
+__device__ __forceinline__ float4 as_f4(Red r) {
+    return make_float4(r.m, r.s, __int_as_float(r.a), 0.f);
+}
+__device__ __forceinline__ Red from_f4(float4 v) { return Red{v.x, v.y, __float_as_int(v.z)}; }
+
+// Warp 0 of the CTA that completed sequence b last: the commit/remask decision for
+// its S <= 32 positions, lane = position.
+__device__ void decide(const UnmaskParams& p, int b) {
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
     const int S = p.S;
-    for (int s = warp; s < S; s += kThreads / 32) {
-        const int row = b * S + s;
-        const bool masked = __ldcg(p.ids + row) == p.mask_id;
-        float conf = 0.f;
-        int tok = 0;
-        if (masked) {
-            const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)row * p.n_chunks);
-            Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
-            for (int c = lane; c < p.n_chunks; c += 32) {
-                const float4 v = __ldcg(pp + c);
-                acc = combine(acc, Red{v.x, v.y, __float_as_int(v.z)});
-            }
-            acc = warp_combine(acc);
-            conf = (acc.s > 0.f) ? 1.0f / acc.s : 0.f;
-            tok = acc.a;
-        }
-        if (lane == 0) {
-            sh_conf[s] = conf;
-            sh_tok[s] = tok;
-            sh_masked[s] = masked ? 1 : 0;
-        }
-    }
-    __syncthreads();
-    if (warp != 0) return;
     const bool in = lane < S;
     const int row = b * S + lane;
-    const bool masked = in && sh_masked[lane] != 0;
-    const float conf = in ? sh_conf[lane] : 0.f;
-    const int tok = in ? sh_tok[lane] : 0;
+    const bool masked = in && __ldcg(p.ids + row) == p.mask_id;
+    float conf = 0.f;
+    int tok = 0;
+    if (masked) {
+        const Red r = from_f4(__ldcg(reinterpret_cast<const float4*>(p.row_res) + row));
+        conf = (r.s > 0.f) ? 1.0f / r.s : 0.f;
+        tok = r.a;
+    }
     const unsigned mball = __ballot_sync(0xffffffffu, masked);
     const int m = __popc(mball);
     const int steps_b = __ldcg(p.steps + b);
@@ -152,20 +140,17 @@ __device__ void decide(const UnmaskParams& p, int b, float* sh_conf, int* sh_tok
     if (lane == 0) {
         if (m > 0) p.steps[b] = steps_b + 1;
         if (p.n_masked) p.n_masked[b] = m - n_take;
-        p.ticket[b] = 0u;
+        p.ticket[p.B * S + b] = 0u;
     }
 }
 
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) unmask_kernel(UnmaskParams p) {
+__global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
     const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
     const int row = b * p.S + s;
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     __shared__ Red red[kThreads / 32];
-    __shared__ int is_last;
-    __shared__ float sh_conf[32];
-    __shared__ int sh_tok[32];
-    __shared__ int sh_masked[32];
 
     const bool masked = __ldcg(p.ids + row) == p.mask_id;
     if (masked) {
@@ -175,18 +160,18 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(UnmaskParams p) {
         const int mid = p.mask_id;
         Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
         if (kVec) {
-            // 4 float4 per thread per batch, ids ascending within the batch.
+            // kBatch float4 per thread per batch, ids ascending within the batch.
             const int n4 = (v1 - v0) >> 2;
             const float4* base = reinterpret_cast<const float4*>(rowp + v0);
             int f = tid;
-            for (; f + 3 * kThreads < n4; f += 4 * kThreads) {
-                float4 q[4];
+            for (; f + (kBatch - 1) * kThreads < n4; f += kBatch * kThreads) {
+                float4 q[kBatch];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) q[u] = ttk::ld_stream_f4(base + f + u * kThreads);
-                float x[16];
-                int id[16];
+                for (int u = 0; u < kBatch; ++u) q[u] = ttk::ld_stream_f4(base + f + u * kThreads);
+                float x[4 * kBatch];
+                int id[4 * kBatch];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kBatch; ++u) {
                     const int i0 = v0 + 4 * (f + u * kThreads);
                     x[4 * u + 0] = q[u].x;
                     x[4 * u + 1] = q[u].y;
@@ -198,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(UnmaskParams p) {
                         if (i0 + e == mid) x[4 * u + e] = -CUDART_INF_F;
                     }
                 }
-                fold<16>(acc, x, id);
+                fold<4 * kBatch>(acc, x, id);
             }
             for (; f < n4; f += kThreads) {
                 const float4 q = ttk::ld_stream_f4(base + f);
@@ -219,54 +204,74 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(UnmaskParams p) {
             }
         }
         acc = warp_combine(acc);
-        if ((tid & 31) == 0) red[tid >> 5] = acc;
-        __syncthreads();
-        if (tid < 32) {
-            Red r = (tid < kThreads / 32) ? red[tid] : Red{-CUDART_INF_F, 0.f, 0x7fffffff};
-            r = warp_combine(r);
-            if (tid == 0) {
-                float4 out;
-                out.x = r.m;
-                out.y = r.s;
-                out.z = __int_as_float(r.a);
-                out.w = 0.f;
-                __stcg(reinterpret_cast<float4*>(p.part + (size_t)row * p.n_chunks + c), out);
-            }
-        }
-    }
-    if (tid == 0) {
-        __threadfence();
-        const unsigned t = atomicAdd(p.ticket + b, 1u);
-        is_last = (t == (unsigned)(p.S * p.n_chunks - 1)) ? 1 : 0;
+        if (lane == 0) red[warp] = acc;
     }
     __syncthreads();
-    if (!is_last) return;
+    if (warp != 0) return;
+
+    // ---- warp 0: chunk partial, then (last chunk of the row) the row result, then
+    // (last row of the sequence) the decision.
+    if (masked) {
+        Red r = (lane < kThreads / 32) ? red[lane] : Red{-CUDART_INF_F, 0.f, 0x7fffffff};
+        r = warp_combine(r);
+        if (lane == 0) __stcg(reinterpret_cast<float4*>(p.part + (size_t)row * p.n_chunks + c), as_f4(r));
+    }
+    unsigned last_chunk = 0;
+    if (lane == 0) {
+        __threadfence();
+        last_chunk = (atomicAdd(p.ticket + row, 1u) == (unsigned)(p.n_chunks - 1)) ? 1u : 0u;
+    }
+    if (__shfl_sync(0xffffffffu, last_chunk, 0) == 0u) return;
     __threadfence();
-    decide(p, b, sh_conf, sh_tok, sh_masked);
+    if (masked) {
+        const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)row * p.n_chunks);
+        Red r{-CUDART_INF_F, 0.f, 0x7fffffff};
+        for (int cc = lane; cc < p.n_chunks; cc += 32) r = combine(r, from_f4(__ldcg(pp + cc)));
+        r = warp_combine(r);
+        if (lane == 0) __stcg(reinterpret_cast<float4*>(p.row_res) + row, as_f4(r));
+    }
+    unsigned last_row = 0;
+    if (lane == 0) {
+        p.ticket[row] = 0u;
+        __threadfence();
+        last_row = (atomicAdd(p.ticket + p.B * p.S + b, 1u) == (unsigned)(p.S - 1)) ? 1u : 0u;
+    }
+    if (__shfl_sync(0xffffffffu, last_row, 0) == 0u) return;
+    __threadfence();
+    decide(p, b);
 }
 
 }  // namespace
 
 size_t unmask_workspace_bytes(int B, int S, int V) {
     // Sized for the smallest chunk (1024 ids), the largest chunk count.
+    const size_t rows = (size_t)B * S;
     const int n_chunks = (V + 1023) / 1024;
-    size_t part = (size_t)B * S * n_chunks * sizeof(UnmaskPartial);
+    size_t part = rows * n_chunks * sizeof(UnmaskPartial);
     part = (part + 255) & ~size_t(255);
-    return part + 256 + (size_t)(B + 1) * sizeof(unsigned int);
+    size_t res = rows * sizeof(UnmaskPartial);
+    res = (res + 255) & ~size_t(255);
+    return part + res + (rows + B + 1) * sizeof(unsigned int);
 }
 
 void unmask_layout(int B, int S, int V, void* ws, UnmaskParams& p) {
-    // Chunk of 8192 ids (32 KiB of fp32) per CTA; fewer rows get smaller chunks so
-    // that the grid still covers the SMs several times.
-    int chunk = 8192;
+    // Chunk of 16384 ids (64 KiB of fp32) per CTA, four batches of four 16-byte loads
+    // per thread, so the reduction tail is paid once per 64 KiB; fewer rows get
+    // smaller chunks so that the grid still covers the SMs several times.
+    int chunk = 16384;
     const long long rows = (long long)B * S;
     while (chunk > 2048 && rows * ((V + chunk - 1) / chunk) < 148LL * 3) chunk >>= 1;
     p.chunk = chunk;
     p.n_chunks = (V + chunk - 1) / chunk;
-    p.part = reinterpret_cast<UnmaskPartial*>(ws);
-    size_t part = (size_t)B * S * ((V + 1023) / 1024) * sizeof(UnmaskPartial);
+    char* w = reinterpret_cast<char*>(ws);
+    size_t part = (size_t)rows * ((V + 1023) / 1024) * sizeof(UnmaskPartial);
     part = (part + 255) & ~size_t(255);
-    p.ticket = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) + part);
+    size_t res = (size_t)rows * sizeof(UnmaskPartial);
+    res = (res + 255) & ~size_t(255);
+    p.part = reinterpret_cast<UnmaskPartial*>(w);
+    p.row_res = reinterpret_cast<UnmaskPartial*>(w + part);
+    p.ticket = reinterpret_cast<unsigned int*>(w + part + res);
+    p.ticket_words = (int)rows + B;
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
