@@ -10,8 +10,8 @@
 // batch, up to four batches per CTA with six CTAs resident per SM), reducing each chunk
 // to (max, lowest argmax, sum of exp).  Completion is
 // counted in two levels, so no ticket sees more than max(chunks per row, S) atomic
-// increments: the last chunk CTA of a row (atomic ticket after a release fence;
-// nothing spins) merges that row's chunk partials into a row result, and the last
+// increments: the last chunk CTA of a row (acquire-release atomic ticket; nothing
+// spins) merges that row's chunk partials into a row result, and the last
 // row of a sequence to finish takes the commit/remask decision for its S <= 32
 // positions with one warp and applies it in place.
 #include <math_constants.h>
@@ -85,6 +85,22 @@ __device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&
 #pragma unroll
     for (int i = 0; i < N; ++i) s += exp2f(fmaf(x[i], kLog2e, off));
     acc.s += s;
+}
+
+// Ticket increment with acquire-release semantics at GPU scope: this thread's earlier
+// writes (its partial) are released, and the writes released by the earlier
+// increments are acquired by the one that sees the final count.
+__device__ __forceinline__ unsigned ticket_add(unsigned* t) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+    return old;
+}
+// Acquire load of a ticket: every lane of the finishing warp synchronises with all
+// the increments before it reads the partials they released.
+__device__ __forceinline__ void ticket_acquire(const unsigned* t) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(t) : "memory");
+    (void)v;
 }
 
 __device__ __forceinline__ float4 as_f4(Red r) {
@@ -217,12 +233,9 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
         if (lane == 0) __stcg(reinterpret_cast<float4*>(p.part + (size_t)row * p.n_chunks + c), as_f4(r));
     }
     unsigned last_chunk = 0;
-    if (lane == 0) {
-        __threadfence();
-        last_chunk = (atomicAdd(p.ticket + row, 1u) == (unsigned)(p.n_chunks - 1)) ? 1u : 0u;
-    }
+    if (lane == 0) last_chunk = (ticket_add(p.ticket + row) == (unsigned)(p.n_chunks - 1)) ? 1u : 0u;
     if (__shfl_sync(0xffffffffu, last_chunk, 0) == 0u) return;
-    __threadfence();
+    ticket_acquire(p.ticket + row);
     if (masked) {
         const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)row * p.n_chunks);
         Red r{-CUDART_INF_F, 0.f, 0x7fffffff};
@@ -230,14 +243,14 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
         r = warp_combine(r);
         if (lane == 0) __stcg(reinterpret_cast<float4*>(p.row_res) + row, as_f4(r));
     }
+    __syncwarp();  // every lane's acquire of the row ticket precedes its reset
     unsigned last_row = 0;
     if (lane == 0) {
         p.ticket[row] = 0u;
-        __threadfence();
-        last_row = (atomicAdd(p.ticket + p.B * p.S + b, 1u) == (unsigned)(p.S - 1)) ? 1u : 0u;
+        last_row = (ticket_add(p.ticket + p.B * p.S + b) == (unsigned)(p.S - 1)) ? 1u : 0u;
     }
     if (__shfl_sync(0xffffffffu, last_row, 0) == 0u) return;
-    __threadfence();
+    ticket_acquire(p.ticket + p.B * p.S + b);
     decide(p, b);
 }
 
