@@ -66,6 +66,27 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+# ------------------------------------------------------------------ replicas
+# Sequences are independent, so N GPUs run N replicas with no data-path collective;
+# the only communication is the barrier and the max of the timed region.
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s replica (distinct synthetic batches per rank)."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """Max of a per-rank float over the process group (the job time is the slowest rank's)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(steps_per_rank: int, world: int, elapsed_max_s: float) -> float:
+    """Whole-job denoise steps/s: every rank ran steps_per_rank steps in at most elapsed_max_s."""
+    return world * steps_per_rank / elapsed_max_s
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -489,7 +510,7 @@ def main():
     from block_wise_mask_tt_b300 import tt
 
     w = workload(args)
-    seed = args.seed + 1000 * rank
+    seed = replica_seed(args.seed, rank)
     wb = Workbench(tt, torch, w, seed)
     if args.kernel_only:
         kernel_only(wb, args.kernel_only, args.reps)
@@ -519,15 +540,13 @@ def main():
         elapsed, launches = run_timed(wb, plan, flush)
     torch.cuda.synchronize()
     if world > 1:
-        t = torch.tensor([elapsed], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, dist, "cuda")
         dist.barrier()
     status = tt.tt_device_status(True)
     if status != 0:
         raise RuntimeError(f"device-side error {status} during the timed region")
 
-    value = world * total_steps / elapsed
+    value = job_throughput(total_steps, world, elapsed)
     peaks, peak_kind = load_peaks()
     ktimes = kernel_times(wb, flush, args.kernel_reps)
     hbm = peaks["hbm_gbs"]
@@ -563,10 +582,8 @@ def main():
     if not args.no_e2e:
         e_el, h2d, d2h = run_e2e(wb, plan, torch, tt)
         if world > 1:
-            t = torch.tensor([e_el], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_el = float(t.item())
-        e2e = {"value": world * total_steps / e_el, "unit": "denoise steps/s",
+            e_el = max_over_ranks(e_el, dist, "cuda")
+        e2e = {"value": job_throughput(total_steps, world, e_el), "unit": "denoise steps/s",
                "h2d_bytes_per_step": int(h2d * len(plan) / total_steps),
                "d2h_bytes_per_step": int(d2h * len(plan) / total_steps)}
 

@@ -32,6 +32,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 __global__ void __launch_bounds__(kThreads) adaln_kernel(AdalnParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     const int row = blockIdx.x;
     const int b = row / p.S;
     if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return;
@@ -110,6 +112,8 @@ __global__ void __launch_bounds__(kThreads) adaln_kernel(AdalnParams p) {
 }
 
 __global__ void count_masked_kernel(InitParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     const int b = blockIdx.x;
     int n = 0;
     for (int s = threadIdx.x; s < p.S; s += 32) n += (p.ids[b * p.S + s] == p.mask_id) ? 1 : 0;
@@ -120,6 +124,8 @@ __global__ void count_masked_kernel(InitParams p) {
 }
 
 __global__ void loop_cond_kernel(LoopCondParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     int active = 0;
     for (int b = threadIdx.x; b < p.B; b += 32)
         active |= (p.n_masked[b] > 0 && p.steps[b] < p.max_steps) ? 1 : 0;
@@ -135,18 +141,15 @@ __global__ void loop_cond_kernel(LoopCondParams p) {
 }  // namespace
 
 cudaError_t launch_adaln(const AdalnParams& p, cudaStream_t stream) {
-    adaln_kernel<<<p.B * p.S, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(adaln_kernel, dim3(p.B * p.S), dim3(kThreads), 0, stream, p);
 }
 
 cudaError_t launch_count_masked(const InitParams& p, cudaStream_t stream) {
-    count_masked_kernel<<<p.B, 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(count_masked_kernel, dim3(p.B), dim3(32), 0, stream, p);
 }
 
 cudaError_t launch_loop_cond(const LoopCondParams& p, cudaStream_t stream) {
-    loop_cond_kernel<<<1, 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(loop_cond_kernel, dim3(1), dim3(32), 0, stream, p);
 }
 
 }  // namespace tti

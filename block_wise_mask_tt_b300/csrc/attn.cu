@@ -99,6 +99,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ AttnSplitParams p,
                       const __grid_constant__ AttnMaps maps) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     using C = Cfg<D>;
     constexpr int NP = C::NP;
     constexpr int NS = C::kStages;
@@ -560,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     constexpr int PER = D / 32;
     constexpr int kBatch = 8;  // accumulators requested together
     const AttnGeom& g = p.g;
@@ -737,10 +741,9 @@ cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cu
     const AttnGeom& g = p.g;
     dim3 grid(g.n_splits * g.n_rg, g.Hkv, g.B);
     if (g.D == 128)
-        attn_split_kernel<128><<<grid, kThreads, Cfg<128>::kBytes, stream>>>(p, maps);
+        return launch_pdl(attn_split_kernel<128>, grid, dim3(kThreads), Cfg<128>::kBytes, stream, p, maps);
     else
-        attn_split_kernel<64><<<grid, kThreads, Cfg<64>::kBytes, stream>>>(p, maps);
-    return cudaGetLastError();
+        return launch_pdl(attn_split_kernel<64>, grid, dim3(kThreads), Cfg<64>::kBytes, stream, p, maps);
 }
 
 cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream) {
@@ -749,10 +752,9 @@ cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream) {
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (g.D == 128)
-        attn_merge_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(p);
+        return launch_pdl(attn_merge_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
     else
-        attn_merge_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(attn_merge_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
 }
 
 }  // namespace tti

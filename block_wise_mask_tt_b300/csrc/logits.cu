@@ -44,6 +44,8 @@ __device__ __forceinline__ float noise(uint32_t r) {
 }
 
 __global__ void __launch_bounds__(kThreads) logits_kernel(LogitsParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
     const int row = b * p.S + s;
     if (p.ids != nullptr && __ldg(p.ids + row) != p.mask_id) return;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(kThreads) logits_kernel(LogitsParams p) {
 }
 
 __global__ void set_dyn_kernel(uint32_t* dyn, uint32_t seed, uint32_t block) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     dyn[0] = seed;
     dyn[1] = block;
 }
@@ -99,14 +103,12 @@ __global__ void set_dyn_kernel(uint32_t* dyn, uint32_t seed, uint32_t block) {
 }  // namespace
 
 cudaError_t launch_set_logits_dyn(uint32_t* dyn, uint32_t seed, int block_index, cudaStream_t stream) {
-    set_dyn_kernel<<<1, 1, 0, stream>>>(dyn, seed, (uint32_t)block_index);
-    return cudaGetLastError();
+    return launch_pdl(set_dyn_kernel, dim3(1), dim3(1), 0, stream, dyn, seed, (uint32_t)block_index);
 }
 
 cudaError_t launch_logits(const LogitsParams& p, cudaStream_t stream) {
     dim3 grid((p.V + kIdsPerCta - 1) / kIdsPerCta, p.S, p.B);
-    logits_kernel<<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(logits_kernel, grid, dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace tti

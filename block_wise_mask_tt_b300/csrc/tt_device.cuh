@@ -20,6 +20,12 @@ __device__ __forceinline__ void report_error(int* err, int code) {
     if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the stream has
+// completed and its memory is visible (a no-op when launched without the attribute),
+// and let the next grid in the stream be scheduled while this one runs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

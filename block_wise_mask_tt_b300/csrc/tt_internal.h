@@ -6,7 +6,28 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace tti {
+
+// Launches `kernel` so that it may be scheduled while the previous grid in the stream
+// is still running (programmatic dependent launch).  Every libtt kernel starts with
+// griddepcontrol.wait, so it reads nothing before its predecessor has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------------------- adaLN
 struct AdalnParams {

@@ -97,10 +97,10 @@ __device__ __forceinline__ unsigned ticket_add(unsigned* t) {
 }
 // Acquire load of a ticket: every lane of the finishing warp synchronises with all
 // the increments before it reads the partials they released.
-__device__ __forceinline__ void ticket_acquire(const unsigned* t) {
+__device__ __forceinline__ unsigned ticket_acquire(const unsigned* t) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(t) : "memory");
-    (void)v;
+    return v;
 }
 
 __device__ __forceinline__ float4 as_f4(Red r) {
@@ -162,6 +162,8 @@ __device__ void decide(const UnmaskParams& p, int b) {
 
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
     const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
     const int row = b * p.S + s;
     const int tid = threadIdx.x;
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
     unsigned last_chunk = 0;
     if (lane == 0) last_chunk = (ticket_add(p.ticket + row) == (unsigned)(p.n_chunks - 1)) ? 1u : 0u;
     if (__shfl_sync(0xffffffffu, last_chunk, 0) == 0u) return;
-    ticket_acquire(p.ticket + row);
+    (void)ticket_acquire(p.ticket + row);
     if (masked) {
         const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)row * p.n_chunks);
         Red r{-CUDART_INF_F, 0.f, 0x7fffffff};
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
         last_row = (ticket_add(p.ticket + p.B * p.S + b) == (unsigned)(p.S - 1)) ? 1u : 0u;
     }
     if (__shfl_sync(0xffffffffu, last_row, 0) == 0u) return;
-    ticket_acquire(p.ticket + p.B * p.S + b);
+    (void)ticket_acquire(p.ticket + p.B * p.S + b);
     decide(p, b);
 }
 
@@ -290,10 +292,9 @@ void unmask_layout(int B, int S, int V, void* ws, UnmaskParams& p) {
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
     dim3 grid(p.n_chunks, p.S, p.B);
     if ((p.V & 3) == 0)
-        unmask_kernel<true><<<grid, kThreads, 0, stream>>>(p);
+        return launch_pdl(unmask_kernel<true>, grid, dim3(kThreads), 0, stream, p);
     else
-        unmask_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(unmask_kernel<false>, grid, dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace tti
