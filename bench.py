@@ -87,6 +87,17 @@ def job_throughput(steps_per_rank: int, world: int, elapsed_max_s: float) -> flo
     return world * steps_per_rank / elapsed_max_s
 
 
+# DRAM bytes (read + write) per call of the dominant kernels, from the ncu captures
+# summarised under profiles/ (denoise_step_*.md: cold-cache, per launch).  Missing
+# entries are reported as null.
+NCU_TRAFFIC = {
+    ("c1_single_B1_L4096_S16_32q2kv_D128", "attn"): 4.47e6 + 4.28e6,
+    ("c1_single_B1_L4096_S16_32q2kv_D128", "unmask"): 8.42e6,
+    ("c2_batched_B32_L8192_S16_32q2kv_D128", "attn"): 274.55e6 + 1.76e6 + 17.06e6,
+    ("c2_batched_B32_L8192_S16_32q2kv_D128", "unmask"): 268.49e6 + 0.12e6,
+}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -565,7 +576,8 @@ def main():
                                  "roofline_us": wb.unmask_bytes_full / (hbm * 1e9) * 1e6,
                                  "frac": um_gbs / hbm, "algorithmic_bytes": wb.unmask_bytes_full},
     }
-    if ktimes["attn"] >= ktimes["unmask"]:
+    dominant = "attn" if ktimes["attn"] >= ktimes["unmask"] else "unmask"
+    if dominant == "attn":
         if attn_bound == "hbm":
             roof = {"kernel": "tt_denoise_attn (split + merge)", "bound": "hbm", "achieved": attn_gbs,
                     "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm}
@@ -575,7 +587,8 @@ def main():
     else:
         roof = {"kernel": "tt_confidence_unmask (first step, all rows masked)", "bound": "hbm",
                 "achieved": um_gbs, "peak": hbm, "unit": "GB/s", "frac": um_gbs / hbm}
-    roof["traffic"] = None
+    roof["traffic"] = NCU_TRAFFIC.get((w.name, dominant))
+    roof["traffic_unit"] = "bytes per call"
     roof["peak_source"] = peak_kind
 
     e2e = None
