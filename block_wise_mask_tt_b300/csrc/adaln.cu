@@ -53,6 +53,12 @@ __global__ void __launch_bounds__(kThreads) adaln_kernel(AdalnParams p) {
     }
     __shared__ float red[kThreads / 32];
     const int n8 = p.H >> 3;
+    // The modulation rows are read only after the two row reductions; pull this
+    // thread's part of them into L2 now so that read does not pay the DRAM latency.
+    for (int c = threadIdx.x; c < n8; c += kThreads) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(sh + 8 * c) : "memory");
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(sc + 8 * c) : "memory");
+    }
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.H);
     float v[kMaxChunks][8];
     float s = 0.f;

@@ -36,9 +36,26 @@ __device__ __forceinline__ uint32_t m3(uint32_t key, uint32_t seed) {
     return h;
 }
 
+// MurmurHash3_x86_32 of a 4-byte key whose first multiplication (key * c1) has
+// already been done: the vocabulary loop advances k by c1 per id instead of
+// multiplying (exact in 32-bit arithmetic).
+__device__ __forceinline__ uint32_t m3_premul(uint32_t k, uint32_t seed) {
+    k = __funnelshift_l(k, k, 15);
+    k *= 0x1B873593u;
+    uint32_t h = seed ^ k;
+    h = __funnelshift_l(h, h, 13);
+    h = h * 5u + 0xE6546B64u;
+    h ^= 4u;  // key length in bytes
+    h ^= h >> 16;
+    h *= 0x85EBCA6Bu;
+    h ^= h >> 13;
+    h *= 0xC2B2AE35u;
+    h ^= h >> 16;
+    return h;
+}
+
 __device__ __forceinline__ float noise(uint32_t r) {
-    const int sum = (int)(r & 0xFFu) + (int)((r >> 8) & 0xFFu) + (int)((r >> 16) & 0xFFu) +
-                    (int)(r >> 24);
+    const int sum = (int)__dp4a(r, 0x01010101u, 0u);  // sum of the four bytes
     // fp32(1/sqrt(4*(256^2-1)/12)) = 0x3BDDB446
     return __fmul_rn(__int2float_rn(sum - 510), __uint_as_float(0x3BDDB446u));
 }
@@ -71,17 +88,21 @@ __global__ void __launch_bounds__(kThreads) logits_kernel(LogitsParams p) {
     const int v0 = c * kIdsPerCta;
     const int v1 = min(p.V, v0 + kIdsPerCta);
     if ((p.V & 3) == 0) {
+        constexpr uint32_t kC1 = 0xCC9E2D51u;
         for (int v = v0 + 4 * threadIdx.x; v < v1; v += 4 * kThreads) {
+            const uint32_t k0 = (uint32_t)v * kC1;
             float4 o;
-            o.x = noise(m3((uint32_t)v + 0u, h));
-            o.y = noise(m3((uint32_t)v + 1u, h));
-            o.z = noise(m3((uint32_t)v + 2u, h));
-            o.w = noise(m3((uint32_t)v + 3u, h));
-            const int d = (int)planted - v;
-            if (d == 0) o.x = __fadd_rn(o.x, boost);
-            if (d == 1) o.y = __fadd_rn(o.y, boost);
-            if (d == 2) o.z = __fadd_rn(o.z, boost);
-            if (d == 3) o.w = __fadd_rn(o.w, boost);
+            o.x = noise(m3_premul(k0, h));
+            o.y = noise(m3_premul(k0 + kC1, h));
+            o.z = noise(m3_premul(k0 + 2u * kC1, h));
+            o.w = noise(m3_premul(k0 + 3u * kC1, h));
+            const unsigned d = planted - (uint32_t)v;
+            if (d < 4u) {  // the planted id is in this group of four
+                if (d == 0) o.x = __fadd_rn(o.x, boost);
+                if (d == 1) o.y = __fadd_rn(o.y, boost);
+                if (d == 2) o.z = __fadd_rn(o.z, boost);
+                if (d == 3) o.w = __fadd_rn(o.w, boost);
+            }
             *reinterpret_cast<float4*>(rowp + v) = o;
         }
     } else {
