@@ -363,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_run = -CUDART_INF_F;
         float l_part = 0.f;  // sum of p over this half's keys
         for (int j = 0; j < nt; ++j) {
-            if (!ttk::mbar_wait(sfull_bar(mt), (uint32_t)(j & 1))) {
-                ok = false;
-                break;
-            }
+            // A wait that runs out is recorded, but the loop goes on: every thread of
+            // the tile must reach the named barriers below the same number of times.
+            // (After a missed phase the later parity waits return at once.)
+            if (!ttk::mbar_wait(sfull_bar(mt), (uint32_t)(j & 1))) ok = false;
             ttk::tc_fence_after();
             const int lim = (j < nblk) ? g.S : ctx - (t0 + j - nblk) * kTileKeys;  // keys >= lim lie outside
             const int k0 = 64 * half;  // first key of this half
@@ -485,20 +485,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         *my_l = ok ? l_part : 0.f;
         named_sync(bar_id, 256);
         const float l = l_part + *other_l;
-        if (!ok) {
-            if (lane_row == 0 && half == 0) ttk::report_error(p.err, ttk::kErrTimeout);
-            if (row_valid && half == 0 && !direct) {
-                const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
-                p.part_ml[2 * pi + 0] = -CUDART_INF_F;
-                p.part_ml[2 * pi + 1] = 0.f;
-            }
-        } else {
+        if (!ok && lane_row == 0 && half == 0) ttk::report_error(p.err, ttk::kErrTimeout);
+        // The tensor-store epilogue is chosen the same way by every thread of the CTA,
+        // and every thread of a tile goes through its named barrier whether or not its
+        // waits ran out (a partial state that ran out is marked empty instead).
+        if (direct ? maps.out_tma != 0 : true) {
             // Epilogue: this half's D/2 columns of the O row go TMEM -> registers ->
-            // shared memory (the Q tiles and the K/V ring are idle once every MMA has
-            // completed) -> one bulk copy.  Single split: normalised bf16 output;
-            // otherwise the fp32 partial accumulator.
+            // 128-row x 128-byte boxes in shared memory (128-byte swizzle, so a warp's
+            // stores of 32 rows fall in different banks; the Q tiles and the K/V ring
+            // are idle once every MMA has completed) -> tensor stores issued by one
+            // thread, whose maps clip rows past R (partials) or past the block's S
+            // positions (output).  Single split: normalised bf16 output; otherwise the
+            // fp32 partial accumulator.
             ttk::tc_fence_after();
-            uint8_t* hrow = smem + (size_t)(r_local * 2 + half) * C::kHalfRow;
+            constexpr int kNbF = D / 32;  // fp32 boxes per row
+            constexpr int kNbH = D / 64;  // bf16 boxes per row
+            const int nb = direct ? kNbH : kNbF;
+            uint8_t* tile_base = smem + (size_t)mt * nb * 16384;
             const float inv = 1.0f / l;
 #pragma unroll
             for (int cc = 0; cc < D / 2; cc += 32) {
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ttk::tmem_ld_wait32(o);
                 if (direct) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 4; ++e) {  // 8 bf16 = one 16-byte chunk
                         uint32_t w[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -515,32 +518,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
                             w[u] = *reinterpret_cast<const uint32_t*>(&pr);
                         }
-                        *reinterpret_cast<uint4*>(hrow + (cc + 8 * e) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+                        const int chunk = (half * (D / 2) + cc + 8 * e) / 8;
+                        uint8_t* dst = tile_base + (chunk >> 3) * 16384 + lane_row * 128 +
+                                       (((chunk & 7) ^ (lane_row & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        *reinterpret_cast<uint4*>(hrow + (cc + 4 * e) * 4) =
-                            make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                    for (int e = 0; e < 8; ++e) {  // 4 fp32 = one 16-byte chunk
+                        const int chunk = (half * (D / 2) + cc + 4 * e) / 4;
+                        uint8_t* dst = tile_base + (chunk >> 3) * 16384 + lane_row * 128 +
+                                       (((chunk & 7) ^ (lane_row & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                    }
+                }
+            }
+            ttk::fence_proxy_async_smem();
+            named_sync(3, 256 * n_mt);  // every row of every tile is staged
+            if (q == 0 && lane_row == 0) {
+                for (int t = 0; t < n_mt; ++t) {
+                    const int row0 = rg * 256 + t * 128;
+                    for (int bx = 0; bx < nb; ++bx) {
+                        const uint32_t src = ttk::smem_u32(smem + (size_t)(t * nb + bx) * 16384);
+                        if (direct)
+                            ttk::tma_store_4d(&maps.out, src, bx * 64, gkv * g.G, row0 / g.G, b);
+                        else
+                            ttk::tma_store_3d(&maps.part, src, bx * 32, row0,
+                                              (b * g.Hkv + gkv) * g.n_splits + split);
+                    }
+                }
+                ttk::bulk_commit();
+                ttk::bulk_wait_read();  // shared memory may be released; the writes land on their own
+            }
+            if (row_valid && half == 0) {
+                if (direct) {
+                    if (p.lse != nullptr) {
+                        const int s = r_glob / g.G, jh = r_glob % g.G;
+                        p.lse[((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh] = (m_run + log2f(l)) * kLn2;
+                    }
+                } else {
+                    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
+                    p.part_ml[2 * pi + 0] = ok ? m_run : -CUDART_INF_F;
+                    p.part_ml[2 * pi + 1] = ok ? l : 0.f;
+                }
+            }
+        } else if (ok) {
+            // Single split with G not dividing 128 (no box covers whole positions):
+            // each half row goes TMEM -> registers -> shared memory -> one bulk copy.
+            // A row stride of D*2 + 16 bytes keeps the 16-byte stores of consecutive
+            // rows in different banks.
+            ttk::tc_fence_after();
+            uint8_t* hrow = smem + (size_t)(r_local * 2 + half) * C::kHalfRow;
+            const float inv = 1.0f / l;
+#pragma unroll
+            for (int cc = 0; cc < D / 2; cc += 32) {
+                uint32_t o[32];
+                ttk::tmem_ld32(tO + half * (D / 2) + cc, o);  // warp-collective: every lane loads
+                ttk::tmem_ld_wait32(o);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                            __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
+                        w[u] = *reinterpret_cast<const uint32_t*>(&pr);
+                    }
+                    *reinterpret_cast<uint4*>(hrow + (cc + 8 * e) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             if (row_valid) {
                 ttk::fence_proxy_async_smem();
-                if (direct) {
-                    const int s = r_glob / g.G, jh = r_glob % g.G;
-                    const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh;
-                    ttk::bulk_store(p.out + orow * D + half * (D / 2), ttk::smem_u32(hrow), D);
-                    ttk::bulk_commit();
-                    if (half == 0 && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
-                } else {
-                    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
-                    ttk::bulk_store(p.part_acc + pi * D + half * (D / 2), ttk::smem_u32(hrow), D * 2);
-                    ttk::bulk_commit();
-                    if (half == 0) {
-                        p.part_ml[2 * pi + 0] = m_run;
-                        p.part_ml[2 * pi + 1] = l;
-                    }
-                }
+                const int s = r_glob / g.G, jh = r_glob % g.G;
+                const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh;
+                ttk::bulk_store(p.out + orow * D + half * (D / 2), ttk::smem_u32(hrow), D);
+                ttk::bulk_commit();
+                if (half == 0 && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
                 ttk::bulk_wait_read();  // shared memory may be released; the writes land on their own
             }
         }

@@ -76,16 +76,22 @@ tt_status device_err_word(int** out) {
 
 // ------------------------------------------------------------------- TMA descriptors
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
 
+// Looks the driver's tensor-map encoder up once.  It takes no lock of its own beyond
+// the once-flag: the block-graph capture calls it while holding g_mu.
 tt_status get_encoder() {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_encode != nullptr) return TT_OK;
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    TT_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
-    if (q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return fail(TT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess && fn != nullptr)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cudaGetDriverEntryPointByVersion");
+    if (g_encode == nullptr) return fail(TT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     return TT_OK;
 }
 
@@ -101,6 +107,19 @@ tt_status encode_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t 
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(TT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return TT_OK;
+}
+
+// Tensor map of `rank` dimensions (dims[0] innermost; strides in bytes for dims 1..),
+// 128-byte swizzle.
+tt_status encode_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                     const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+    TT_TRY(get_encoder());
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return TT_OK;
 }
@@ -185,6 +204,26 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     acc_bytes = (acc_bytes + 255) & ~size_t(255);
     float* part_acc = static_cast<float*>(ws);
     float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+    // Epilogue store maps: partial states when the context is split, else the output
+    // itself (when G divides 128, so that a 128-row tile covers whole positions).
+    tti::AttnMaps maps = pl.maps;
+    maps.part = maps.kb;  // placeholders for the map that is not used
+    maps.out = maps.kb;
+    maps.out_tma = 0;
+    if (g.n_splits > 1) {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.R,
+                                    (cuuint64_t)g.B * g.Hkv * g.n_splits};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)g.R * g.D * 4};
+        const cuuint32_t box[3] = {32, 128, 1};
+        TT_TRY(encode_map(&maps.part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part_acc, dims, strides, box));
+    } else if (128 % g.G == 0) {
+        const cuuint64_t dims[4] = {(cuuint64_t)g.D, (cuuint64_t)g.Hq, (cuuint64_t)g.S, (cuuint64_t)g.B};
+        const cuuint64_t strides[3] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.Hq * g.D * 2,
+                                       (cuuint64_t)g.S * g.Hq * g.D * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)g.G, (cuuint32_t)(128 / g.G), 1};
+        TT_TRY(encode_map(&maps.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, box));
+        maps.out_tma = 1;
+    }
     tti::AttnSplitParams sp;
     sp.g = g;
     sp.q = static_cast<const uint16_t*>(q);
@@ -196,7 +235,7 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     sp.out = static_cast<uint16_t*>(out);
     sp.lse = lse;
     sp.err = err;
-    TT_CUDA(tti::launch_attn_split(sp, pl.maps, st));
+    TT_CUDA(tti::launch_attn_split(sp, maps, st));
     if (g.n_splits > 1) {
         tti::AttnMergeParams mp;
         mp.g = g;

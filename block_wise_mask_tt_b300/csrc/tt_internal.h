@@ -133,6 +133,12 @@ struct AttnMaps {
     CUtensorMap v;   // context values
     CUtensorMap kb;  // the block's own keys, bf16 [B*S][Hkv][D], same box
     CUtensorMap vb;  // the block's own values
+    // Epilogue stores (128-byte swizzle): the fp32 partial states [splits*B*Hkv][R][D]
+    // with box (32, 128, 1), and the bf16 output [B][S][Hq][D] with box
+    // (64, G, 128/G, 1) when G divides 128 (out_tma).
+    CUtensorMap part;
+    CUtensorMap out;
+    int out_tma;
 };
 cudaError_t attn_split_prepare(int D);  // sets the kernel's shared-memory limit on this device
 cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cudaStream_t stream);
