@@ -12,7 +12,9 @@ Sources ("Nemotron-Labs-TwoTower" wiki page unless stated otherwise):
   "Ablations" (adaptive layer normalization on the diffusion timestep);
 * denoise attention - section "Architecture" (block queries attend over the context
   tower's layer-i cache followed by the block's own keys, bidirectional in the block);
-* confidence unmasking and the timestep rule - section "Block-wise generation".
+* confidence unmasking and the timestep rule - section "Block-wise generation";
+* sampler variants (temperature, mock-AR, predict-and-noise) - sections
+  "Block-wise generation" and "Release history and artifacts" and the opening summary.
 
 Every function computes the plain definition: no blocking, no fusion, no reordering
 beyond what the definition states.  Readings where the pages are silent are listed
@@ -22,6 +24,7 @@ from .adaln import adaln_modulate
 from .attention import denoise_attention, denoise_attention_rows, context_kv
 from .unmask import row_confidence, unmask_step
 from .loop import denoise_block, denoise_block_batch
+from .samplers import sampler_step, sampler_block, row_confidence_t
 
 __all__ = [
     "adaln_modulate",
@@ -32,4 +35,7 @@ __all__ = [
     "unmask_step",
     "denoise_block",
     "denoise_block_batch",
+    "sampler_step",
+    "sampler_block",
+    "row_confidence_t",
 ]

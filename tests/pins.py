@@ -335,3 +335,106 @@ UNMASK_ROW_CHECKS = (check_conf_two_valued, check_conf_vs_scipy, check_mask_neve
 UNMASK_STEP_CHECKS = (check_threshold_inclusive,)
 BLOCK_CHECKS = (check_gamma_zero_one_step, check_gamma_above_one_takes_s_steps,
                 check_floor_ceil_rule, check_frozen_and_bounded, check_floor_ties_lower_position)
+
+
+# ----------------------------------------------------------------------------------
+# sampler variants (temperature, mock-AR, predict-and-noise)
+# ----------------------------------------------------------------------------------
+# Each check takes sampler_step(logits, ids, steps, mask_id, T, kind, gamma,
+# temperature, commit_step) from oracle.samplers (or a mutated copy).
+SAMPLER_CONFIDENCE, SAMPLER_MOCK_AR, SAMPLER_PREDICT_NOISE = 0, 1, 2
+
+
+def _run_block(step_fn, S, T, mask_id, logits_fn, kind, gamma=0.8, temperature=1.0):
+    ids = np.full(S, mask_id, np.int64)
+    cs = np.zeros(S, np.uint8)
+    steps = 0
+    per_step = []
+    while np.any(ids == mask_id) and steps < 64:
+        k = steps
+        r = step_fn(lambda pos: logits_fn(k, pos), ids, steps, mask_id, T, kind, gamma, temperature, cs)
+        per_step.append(r)
+        ids, cs, steps = r["ids"], r["commit_step"], r["steps"]
+    return ids, cs, steps, per_step
+
+
+def check_temperature_closed_form(step_fn):
+    """Two-valued row (a at one id, b at the other V-2, the mask id excluded):
+    conf = 1 / (1 + (V-2) exp((b-a)/tau)); the token is the argmax for every tau."""
+    V, mask = 40, 5
+    for tau in (0.1, 0.5, 1.0, 3.0):
+        a, b = 2.0, 0.5
+        row = np.full(V, b, np.float32)
+        row[17] = a
+        row[mask] = 50.0  # largest, but excluded
+        logits = np.tile(row, (3, 1))
+        ids = np.array([mask, 9, mask])
+        r = step_fn(logits, ids, 0, mask, 16, SAMPLER_CONFIDENCE, 2.0, tau, None)
+        want = 1.0 / (1.0 + (V - 2) * math.exp((b - a) / tau))
+        assert abs(r["conf"][0] - want) <= 1e-12 * want
+        assert r["tok"][0] == 17 and r["tok"][2] == 17 and r["conf"][1] == 0.0
+
+
+def check_temperature_vs_scipy(step_fn):
+    from scipy.special import softmax
+    rng = np.random.default_rng(3)
+    V, mask, S = 300, 3, 6
+    logits = rng.standard_normal((S, V)).astype(np.float32) * 2
+    for tau in (0.25, 1.0, 2.5):
+        r = step_fn(logits, np.full(S, mask), 0, mask, S, SAMPLER_CONFIDENCE, 2.0, tau, None)
+        for i in range(S):
+            l = logits[i].astype(np.float64).copy()
+            l[mask] = -np.inf
+            p = softmax(l / tau)
+            assert abs(r["conf"][i] - p.max()) <= 1e-12
+            assert r["tok"][i] == int(np.argmax(l))
+
+
+def check_temperature_one_is_plain_confidence(step_fn):
+    """tau = 1 with gamma = 0 commits the whole block in one step; gamma > 1 one per step."""
+    ids, cs, steps, _ = _run_block(step_fn, 8, 8, 3, _random_logits_fn(5, 256, 3), SAMPLER_CONFIDENCE, 0.0)
+    assert steps == 1 and np.all(cs == 1)
+    ids, cs, steps, _ = _run_block(step_fn, 8, 8, 3, _random_logits_fn(6, 256, 3), SAMPLER_CONFIDENCE, 1.01)
+    assert steps == 8 and sorted(cs.tolist()) == list(range(1, 9))
+
+
+def check_mock_ar_left_to_right(step_fn):
+    """One token per step, in position order: commit_step[i] = i + 1, S steps."""
+    for S in (1, 7, 16):
+        ids, cs, steps, per = _run_block(step_fn, S, S, 3, _random_logits_fn(40 + S, 256, 3), SAMPLER_MOCK_AR)
+        assert steps == S
+        assert cs.tolist() == list(range(1, S + 1))
+        assert np.all(ids != 3)
+        assert all(int(r["commit"].sum()) == 1 for r in per)
+
+
+def check_mock_ar_skips_decoded_positions(step_fn):
+    mask = 3
+    logits = np.zeros((5, 16), np.float32)
+    ids = np.array([7, mask, 9, mask, mask])
+    r = step_fn(logits, ids, 0, mask, 5, SAMPLER_MOCK_AR, 0.8, 1.0, None)
+    assert r["commit"].tolist() == [0, 1, 0, 0, 0]
+    assert r["ids"][0] == 7 and r["ids"][2] == 9
+
+
+def check_predict_noise_schedule(step_fn):
+    """Linear schedule: floor(S (T - k - 1) / T) stay masked after step k (at least one
+    commit per step); the committed positions are the most confident (by scipy)."""
+    from scipy.special import softmax
+    for S, T, counts in ((16, 4, [4, 4, 4, 4]), (16, 16, [1] * 16), (16, 5, [4, 3, 3, 3, 3]),
+                         (8, 3, [3, 3, 2])):
+        fn = _random_logits_fn(60 + T, 256, 3)
+        ids, cs, steps, per = _run_block(step_fn, S, T, 3, fn, SAMPLER_PREDICT_NOISE)
+        assert [int(r["commit"].sum()) for r in per] == counts
+        assert steps == T and np.all(ids != 3)
+        # first step: the committed set is the top-k by confidence
+        lg = fn(0, np.arange(S)).astype(np.float64)
+        lg[:, 3] = -np.inf
+        conf = np.array([softmax(row).max() for row in lg])
+        top = sorted(range(S), key=lambda i: (-conf[i], i))[:counts[0]]
+        assert sorted(np.flatnonzero(per[0]["commit"]).tolist()) == sorted(top)
+
+
+SAMPLER_CHECKS = [check_temperature_closed_form, check_temperature_vs_scipy,
+                  check_temperature_one_is_plain_confidence, check_mock_ar_left_to_right,
+                  check_mock_ar_skips_decoded_positions, check_predict_noise_schedule]

@@ -230,3 +230,71 @@ def test_step_mutant_rejected(name):
     block_ok = not _rejected(checks, _block_with(kw))
     step_ok = not _rejected(pins.UNMASK_STEP_CHECKS, lambda *a, **k: _step_generic(*a, **k, **kw))
     assert not (block_ok and step_ok)
+
+
+# ----------------------------------------------------------------------------------
+# sampler variants
+# ----------------------------------------------------------------------------------
+def _sampler_generic(logits, ids, steps, mask_id, T, kind=0, gamma=0.8, temperature=1.0,
+                     commit_step=None, *, temp_multiplies=False, ar_rightmost=False,
+                     ar_most_confident=False, schedule_off_by_one=False, pn_least=False):
+    import math
+    ids = np.array(ids, dtype=np.int64)
+    S = ids.size
+    masked = [i for i in range(S) if ids[i] == mask_id]
+    m = len(masked)
+    cs = np.zeros(S, np.uint8) if commit_step is None else np.array(commit_step, np.uint8)
+    conf = np.zeros(S)
+    tok = np.full(S, -1, dtype=np.int64)
+    commit = np.zeros(S, np.uint8)
+    if m == 0:
+        return dict(ids=ids, commit=commit, conf=conf, tok=tok, n_masked=0, steps=steps,
+                    commit_step=cs, k_min=0)
+    rows = logits(masked) if callable(logits) else np.asarray(logits)[masked]
+    for j, i in enumerate(masked):
+        a = np.asarray(rows[j], np.float64).copy()
+        a[mask_id] = -np.inf
+        tok[i] = int(np.argmax(a))
+        z = (a - a[tok[i]]) * temperature if temp_multiplies else (a - a[tok[i]]) / temperature
+        conf[i] = 1.0 / float(np.sum(np.exp(z)))
+    by_conf = sorted(masked, key=lambda i: (-conf[i], i))
+    if kind == 0:
+        left = T - steps
+        k_min = m if left <= 0 else int(math.ceil(m / left))
+        chosen = [i for i in masked if conf[i] >= gamma]
+        if len(chosen) < k_min:
+            chosen = by_conf[:k_min]
+    elif kind == 1:
+        k_min = 1
+        chosen = [masked[-1]] if ar_rightmost else [by_conf[0]] if ar_most_confident else [masked[0]]
+    else:
+        left = T - steps - (0 if schedule_off_by_one else 1)
+        keep = 0 if left <= 0 else (S * left) // T
+        k_min = min(m, max(1, m - keep))
+        chosen = (by_conf[::-1] if pn_least else by_conf)[:k_min]
+    steps += 1
+    for i in chosen:
+        ids[i] = tok[i]
+        commit[i] = 1
+        cs[i] = steps
+    return dict(ids=ids, commit=commit, conf=conf, tok=tok, n_masked=m - len(chosen),
+                steps=steps, commit_step=cs, k_min=k_min)
+
+
+SAMPLER_MUTANTS = {
+    "temperature_multiplies": dict(temp_multiplies=True),
+    "mock_ar_rightmost": dict(ar_rightmost=True),
+    "mock_ar_most_confident": dict(ar_most_confident=True),
+    "schedule_off_by_one": dict(schedule_off_by_one=True),
+    "predict_noise_least_confident": dict(pn_least=True),
+}
+
+
+def test_sanity_generic_sampler_passes():
+    assert not _rejected(pins.SAMPLER_CHECKS, lambda *a: _sampler_generic(*a))
+
+
+@pytest.mark.parametrize("name", sorted(SAMPLER_MUTANTS))
+def test_sampler_mutant_rejected(name):
+    kw = SAMPLER_MUTANTS[name]
+    assert _rejected(pins.SAMPLER_CHECKS, lambda *a: _sampler_generic(*a, **kw))

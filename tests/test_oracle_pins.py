@@ -73,3 +73,24 @@ def test_operating_point_golden():
         assert w.mask_id == g["mask_token_id"]["value"]
     r = oracle.denoise_block(16, 16, 3, 0.8, pins._random_logits_fn(0, 64, 3))
     assert r["trace"][0]["t"] == g["first_timestep"]["value"]
+
+
+@pytest.mark.parametrize("check", pins.SAMPLER_CHECKS, ids=lambda f: f.__name__)
+def test_samplers(check):
+    from oracle.samplers import sampler_step
+    check(sampler_step)
+
+
+def test_sampler_confidence_equals_unmask_step():
+    """The confidence sampler at tau = 1 is the main oracle's step."""
+    import numpy as np
+    from oracle.samplers import sampler_step
+    fn = pins._random_logits_fn(9, 512, 3)
+    ids = np.full(16, 3)
+    ids[[1, 4]] = [10, 11]
+    lg = fn(2, np.arange(16))
+    a = oracle.unmask_step(lg, ids, 2, 3, 0.8, 16)
+    b = sampler_step(lg, ids, 2, 3, 16, 0, 0.8, 1.0)
+    for k in ("ids", "commit", "commit_step", "n_masked", "steps", "k_min"):
+        assert np.array_equal(a[k], b[k]), k
+    assert np.allclose(a["conf"], b["conf"], rtol=1e-15, atol=0)
