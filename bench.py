@@ -48,6 +48,11 @@ def parse_args():
     ap.add_argument("--impl", choices=("tt", "reference"), default="tt")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gamma", type=float, default=None)
+    ap.add_argument("--sampler", choices=("confidence", "mock_ar", "predict_noise"),
+                    default="confidence",
+                    help="unmask rule: confidence unmasking (the main sampler), mock-AR (one "
+                         "token per step, left to right) or predict-and-noise (linear schedule)")
+    ap.add_argument("--temperature", type=float, default=1.0)
     ap.add_argument("--kernel-reps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -182,10 +187,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU workload
+SAMPLERS = {"confidence": 0, "mock_ar": 1, "predict_noise": 2}
+
+
 class Workbench:
     """Device-resident inputs, state and buffers for one replica of the workload."""
 
-    def __init__(self, tt, torch, w: synth.Workload, seed: int):
+    def __init__(self, tt, torch, w: synth.Workload, seed: int, sampler: int = 0,
+                 temperature: float = 1.0):
         self.tt, self.torch, self.w, self.seed = tt, torch, w, seed
         t0 = time.time()
         self.inp = synth.make_attention_inputs(w, seed)
@@ -218,7 +227,8 @@ class Workbench:
             conf=T.empty((B, S), dtype=T.float32, device="cuda"),
             commit=T.empty((B, S), dtype=T.uint8, device="cuda"))
         self.desc = tt.step_desc(self.dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps,
-                                 seed, 0, w.logits_kind, w.boost_lo, w.boost_hi)
+                                 seed, 0, w.logits_kind, w.boost_lo, w.boost_hi, sampler=sampler,
+                                 temperature=temperature)
         self.ts = tt.step_tensors(**self.t)
         self.ws = tt.workspace(tt.tt_denoise_workspace(self.desc))
         ctx = self.inp["ctx_len"].astype(np.int64)
@@ -522,7 +532,7 @@ def main():
 
     w = workload(args)
     seed = replica_seed(args.seed, rank)
-    wb = Workbench(tt, torch, w, seed)
+    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature)
     if args.kernel_only:
         kernel_only(wb, args.kernel_only, args.reps)
         return
@@ -617,6 +627,7 @@ def main():
         "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
                    "D": w.D, "H": w.H, "V": w.V, "gamma": w.gamma, "paged": w.paged,
                    "bench_step": "one denoise step of the whole batch",
+                   "sampler": args.sampler, "temperature": args.temperature,
                    "blocks_timed": len(plan), "whole_blocks": blocks_full,
                    "tokens_per_step": w.B * w.S * blocks_full / max(1, sum(t for _, n, t in plan if t == n)),
                    "l2": "flushed (512 MiB write) before every timed block, outside the events",

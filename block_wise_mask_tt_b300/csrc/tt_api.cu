@@ -44,6 +44,10 @@ tt_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// exp2 scale of the unmask softmax at temperature tau: log2(e) / tau (exactly the
+// plain constant at tau = 1).
+float temp_scale(float tau) { return 1.4426950408889634f / tau; }
+
 tt_status need_ptr(const void* p, const char* name, bool align = true) {
     if (p == nullptr) return fail(TT_ERR_INVALID_ARG, "%s is null", name);
     if (align && !aligned16(p)) return fail(TT_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
@@ -278,6 +282,10 @@ tt_status plan_step(const tt_step_desc* d, StepPlan& sp) {
     if (d->mask_id < 0 || d->mask_id >= d->V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
     if (!(d->ln_eps >= 0.f)) return fail(TT_ERR_INVALID_ARG, "ln_eps must be >= 0");
     if (d->logits.kind != 0 && d->logits.kind != 1) return fail(TT_ERR_INVALID_ARG, "logits.kind must be 0 or 1");
+    if (d->sampler < TT_SAMPLER_CONFIDENCE || d->sampler > TT_SAMPLER_PREDICT_NOISE)
+        return fail(TT_ERR_INVALID_ARG, "sampler must be a tt_sampler_kind");
+    if (!(d->temperature > 0.f) || !(d->temperature < 1e30f))
+        return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
     sp.attn_ws = (tti::attn_workspace_bytes(sp.attn.g) + 255) & ~size_t(255);
     sp.unmask_ws_off = sp.attn_ws;
     sp.dyn_off = (sp.attn_ws + tti::unmask_workspace_bytes(d->attn.B, d->attn.S, d->V) + 255) &
@@ -355,6 +363,8 @@ tt_status enqueue_step(const tt_step_desc* d, const tt_step_tensors* t, const St
     up.mask_id = d->mask_id;
     up.gamma = d->gamma;
     up.max_steps = d->max_steps;
+    up.mode = d->sampler;
+    up.temp_scale = temp_scale(d->temperature);
     tti::unmask_layout(B, S, d->V, static_cast<char*>(ws) + sp.unmask_ws_off, up);
     up.err = err;
     TT_CUDA(tti::launch_unmask(up, st));
@@ -638,6 +648,50 @@ tt_status tt_confidence_unmask(const float* logits, int32_t* ids, int32_t* n_mas
     p.mask_id = mask_id;
     p.gamma = gamma;
     p.max_steps = max_steps;
+    p.mode = TT_SAMPLER_CONFIDENCE;
+    p.temp_scale = temp_scale(1.0f);
+    tti::unmask_layout(B, S, V, workspace, p);
+    p.err = err;
+    TT_CUDA(tti::launch_unmask(p, reinterpret_cast<cudaStream_t>(stream)));
+    return TT_OK;
+}
+
+tt_status tt_sampler_unmask(const float* logits, int32_t* ids, int32_t* n_masked, int32_t* steps,
+                            float* conf, uint8_t* commit, uint8_t* commit_step, int B, int S, int V,
+                            int32_t mask_id, const tt_sampler* sampler, void* workspace,
+                            size_t workspace_bytes, tt_stream_t stream) {
+    if (sampler == nullptr) return fail(TT_ERR_INVALID_ARG, "sampler is null");
+    TT_TRY(check_vocab(B, S, V));
+    if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
+    if (sampler->kind < TT_SAMPLER_CONFIDENCE || sampler->kind > TT_SAMPLER_PREDICT_NOISE)
+        return fail(TT_ERR_INVALID_ARG, "sampler kind must be a tt_sampler_kind");
+    if (sampler->max_steps < 1 || sampler->max_steps > 255)
+        return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
+    if (sampler->gamma != sampler->gamma) return fail(TT_ERR_INVALID_ARG, "gamma is NaN");
+    if (!(sampler->temperature > 0.f) || !(sampler->temperature < 1e30f))
+        return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
+    TT_TRY(need_ptr(logits, "logits"));
+    TT_TRY(need_ptr(ids, "ids", false));
+    TT_TRY(need_ptr(steps, "steps", false));
+    TT_TRY(check_ws(workspace, workspace_bytes, tti::unmask_workspace_bytes(B, S, V)));
+    int* err = nullptr;
+    TT_TRY(device_err_word(&err));
+    tti::UnmaskParams p;
+    p.logits = logits;
+    p.ids = ids;
+    p.n_masked = n_masked;
+    p.steps = steps;
+    p.conf = conf;
+    p.commit = commit;
+    p.commit_step = commit_step;
+    p.B = B;
+    p.S = S;
+    p.V = V;
+    p.mask_id = mask_id;
+    p.gamma = sampler->gamma;
+    p.max_steps = sampler->max_steps;
+    p.mode = sampler->kind;
+    p.temp_scale = temp_scale(sampler->temperature);
     tti::unmask_layout(B, S, V, workspace, p);
     p.err = err;
     TT_CUDA(tti::launch_unmask(p, reinterpret_cast<cudaStream_t>(stream)));
@@ -680,6 +734,8 @@ tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids, int32_
     p.mask_id = mask_id;
     p.gamma = gamma;
     p.max_steps = max_steps;
+    p.mode = TT_SAMPLER_CONFIDENCE;
+    p.temp_scale = temp_scale(1.0f);
     tti::unmask_layout(B, S, V, scratch, p);
     p.err = err;
     // The array keeps whatever the previous call left; the tickets must start at zero.

@@ -80,6 +80,8 @@ struct UnmaskParams {
     int32_t mask_id;
     float gamma;
     int max_steps;
+    int mode;           // tt_sampler_kind
+    float temp_scale;   // log2(e) / temperature
     int chunk;      // vocabulary entries per CTA (multiple of 1024)
     int n_chunks;
     UnmaskPartial* part;     // [B*S][n_chunks]: one per (row, vocabulary chunk)

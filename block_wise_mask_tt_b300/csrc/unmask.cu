@@ -26,7 +26,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBatch = 4;  // 16-byte loads per thread per batch
-constexpr float kLog2e = 1.4426950408889634f;
 
 struct Red {
     float m;
@@ -34,9 +33,9 @@ struct Red {
     int a;
 };
 
-// Merge two (max, sum-of-exp relative to max, argmax) triples; equal maxima keep
-// the lower id.
-__device__ __forceinline__ Red combine(Red x, Red y) {
+// Merge two (max, sum of 2^((x - max) * ts), argmax) triples, ts = log2(e) /
+// temperature; equal maxima keep the lower id.
+__device__ __forceinline__ Red combine(Red x, Red y, float ts) {
     Red r;
     r.m = fmaxf(x.m, y.m);
     if (r.m == -CUDART_INF_F) {
@@ -44,19 +43,19 @@ __device__ __forceinline__ Red combine(Red x, Red y) {
         r.a = min(x.a, y.a);
         return r;
     }
-    r.s = x.s * exp2f((x.m - r.m) * kLog2e) + y.s * exp2f((y.m - r.m) * kLog2e);
+    r.s = x.s * exp2f((x.m - r.m) * ts) + y.s * exp2f((y.m - r.m) * ts);
     r.a = (x.m > y.m) ? x.a : (y.m > x.m) ? y.a : min(x.a, y.a);
     return r;
 }
 
-__device__ __forceinline__ Red warp_combine(Red v) {
+__device__ __forceinline__ Red warp_combine(Red v, float ts) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         Red w;
         w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
         w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
         w.a = __shfl_xor_sync(0xffffffffu, v.a, o);
-        v = combine(v, w);
+        v = combine(v, w, ts);
     }
     return v;
 }
@@ -64,7 +63,7 @@ __device__ __forceinline__ Red warp_combine(Red v) {
 // Folds one batch of values (ids ascending in the order given) into the running
 // triple of this thread.
 template <int N>
-__device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&id)[N]) {
+__device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&id)[N], float ts) {
     float bm = x[0];
     int ba = id[0];
 #pragma unroll
@@ -75,15 +74,15 @@ __device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&
         }
     }
     if (bm > acc.m) {
-        acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - bm) * kLog2e);
+        acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - bm) * ts);
         acc.m = bm;
         acc.a = ba;
     }
     if (acc.m == -CUDART_INF_F) return;
-    const float off = -acc.m * kLog2e;
+    const float off = -acc.m * ts;
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) s += exp2f(fmaf(x[i], kLog2e, off));
+    for (int i = 0; i < N; ++i) s += exp2f(fmaf(x[i], ts, off));
     acc.s += s;
 }
 
@@ -128,20 +127,39 @@ __device__ void decide(const UnmaskParams& p, int b) {
     const int steps_b = __ldcg(p.steps + b);
     bool take = false;
     if (m > 0) {
-        const int left = p.max_steps - steps_b;
-        const int k_min = (left > 0) ? (m + left - 1) / left : m;
-        const bool above = masked && conf >= p.gamma;
-        const unsigned aball = __ballot_sync(0xffffffffu, above);
-        if (__popc(aball) >= k_min) {
-            take = above;
-        } else {
+        // rank = this position's place among the masked ones by confidence (higher
+        // first, equal confidences by lower position)
+        auto rank_of = [&]() {
             int rank = 0;
             for (int j = 0; j < 32; ++j) {
                 const float cj = __shfl_sync(0xffffffffu, conf, j);
                 const bool mj = (mball >> j) & 1u;
                 rank += (mj && (cj > conf || (cj == conf && j < lane))) ? 1 : 0;
             }
-            take = masked && rank < k_min;
+            return rank;
+        };
+        if (p.mode == 1) {
+            // mock-AR: the leftmost masked position
+            take = masked && lane == __ffs(mball) - 1;
+        } else if (p.mode == 2) {
+            // predict-and-noise: the linear schedule leaves floor(S (T - steps - 1) / T)
+            // masked; the most confident of the rest are committed (at least one)
+            const int left = p.max_steps - steps_b - 1;
+            const int keep = (left <= 0) ? 0 : (S * left) / p.max_steps;
+            const int k = min(m, max(1, m - keep));
+            const int rank = rank_of();
+            take = masked && rank < k;
+        } else {
+            const int left = p.max_steps - steps_b;
+            const int k_min = (left > 0) ? (m + left - 1) / left : m;
+            const bool above = masked && conf >= p.gamma;
+            const unsigned aball = __ballot_sync(0xffffffffu, above);
+            if (__popc(aball) >= k_min) {
+                take = above;
+            } else {
+                const int rank = rank_of();
+                take = masked && rank < k_min;
+            }
         }
     }
     const int n_take = __popc(__ballot_sync(0xffffffffu, take));
@@ -201,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
                         if (i0 + e == mid) x[4 * u + e] = -CUDART_INF_F;
                     }
                 }
-                fold<4 * kBatch>(acc, x, id);
+                fold<4 * kBatch>(acc, x, id, p.temp_scale);
             }
             for (; f < n4; f += kThreads) {
                 const float4 q = ttk::ld_stream_f4(base + f);
@@ -211,17 +229,17 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (id[e] == mid) x[e] = -CUDART_INF_F;
-                fold<4>(acc, x, id);
+                fold<4>(acc, x, id, p.temp_scale);
             }
         } else {
             for (int v = v0 + tid; v < v1; v += kThreads) {
                 float x[1] = {__ldcs(rowp + v)};
                 int id[1] = {v};
                 if (v == mid) x[0] = -CUDART_INF_F;
-                fold<1>(acc, x, id);
+                fold<1>(acc, x, id, p.temp_scale);
             }
         }
-        acc = warp_combine(acc);
+        acc = warp_combine(acc, p.temp_scale);
         if (lane == 0) red[warp] = acc;
     }
     __syncthreads();
@@ -231,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
     // (last row of the sequence) the decision.
     if (masked) {
         Red r = (lane < kThreads / 32) ? red[lane] : Red{-CUDART_INF_F, 0.f, 0x7fffffff};
-        r = warp_combine(r);
+        r = warp_combine(r, p.temp_scale);
         if (lane == 0) __stcg(reinterpret_cast<float4*>(p.part + (size_t)row * p.n_chunks + c), as_f4(r));
     }
     unsigned last_chunk = 0;
@@ -241,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
     if (masked) {
         const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)row * p.n_chunks);
         Red r{-CUDART_INF_F, 0.f, 0x7fffffff};
-        for (int cc = lane; cc < p.n_chunks; cc += 32) r = combine(r, from_f4(__ldcg(pp + cc)));
-        r = warp_combine(r);
+        for (int cc = lane; cc < p.n_chunks; cc += 32) r = combine(r, from_f4(__ldcg(pp + cc)), p.temp_scale);
+        r = warp_combine(r, p.temp_scale);
         if (lane == 0) __stcg(reinterpret_cast<float4*>(p.row_res) + row, as_f4(r));
     }
     __syncwarp();  // every lane's acquire of the row ticket precedes its reset

@@ -53,7 +53,16 @@ class tt_step_desc(ctypes.Structure):
     _fields_ = [("attn", tt_attn_dims), ("H", ctypes.c_int), ("V", ctypes.c_int),
                 ("mask_id", ctypes.c_int32), ("gamma", ctypes.c_float),
                 ("max_steps", ctypes.c_int), ("ln_eps", ctypes.c_float),
-                ("logits", tt_logits_spec)]
+                ("logits", tt_logits_spec), ("sampler", ctypes.c_int),
+                ("temperature", ctypes.c_float)]
+
+
+SAMPLER_CONFIDENCE, SAMPLER_MOCK_AR, SAMPLER_PREDICT_NOISE = 0, 1, 2
+
+
+class tt_sampler(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("gamma", ctypes.c_float), ("temperature", ctypes.c_float),
+                ("max_steps", ctypes.c_int)]
 
 
 _STEP_TENSOR_FIELDS = ("x", "shift_table", "scale_table", "q", "k_blk", "v_blk", "k_ctx", "v_ctx",
@@ -81,6 +90,8 @@ _SIGS = {
     "tt_confidence_unmask_workspace": (ctypes.c_size_t, [_I, _I, _I]),
     "tt_confidence_unmask": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
                                   ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+    "tt_sampler_unmask": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
+                               ctypes.POINTER(tt_sampler), _P, ctypes.c_size_t, _P]),
     "tt_confidence_unmask_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
                                           ctypes.c_float, _I, _P]),
     "tt_denoise_workspace": (ctypes.c_size_t, [ctypes.POINTER(tt_step_desc)]),
@@ -206,6 +217,18 @@ def tt_confidence_unmask(logits, ids, steps, B, S, V, mask_id, gamma, max_steps,
         int(max_steps), ws.data_ptr(), ws.numel(), _stream(stream)))
 
 
+def tt_sampler_unmask(logits, ids, steps, B, S, V, mask_id, sampler: tt_sampler, n_masked=None,
+                      conf=None, commit=None, commit_step=None, ws=None, stream=None) -> None:
+    if ws is None:
+        ws = workspace(tt_confidence_unmask_workspace(B, S, V), logits.device)
+    _check(lib.tt_sampler_unmask(
+        _ptr(logits, "logits", _F32, B * S * V), _ptr(ids, "ids", _I32, B * S),
+        _ptr(n_masked, "n_masked", _I32, B), _ptr(steps, "steps", _I32, B),
+        _ptr(conf, "conf", _F32, B * S), _ptr(commit, "commit", _U8, B * S),
+        _ptr(commit_step, "commit_step", _U8, B * S), B, S, V, int(mask_id),
+        ctypes.byref(sampler), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
 def tt_confidence_unmask_noalloc(logits, ids, steps, B, S, V, mask_id, gamma, max_steps,
                                  n_masked=None, conf=None, commit=None, commit_step=None,
                                  stream=None) -> None:
@@ -220,10 +243,11 @@ def tt_confidence_unmask_noalloc(logits, ids, steps, B, S, V, mask_id, gamma, ma
 
 
 def step_desc(attn: tt_attn_dims, H, V, mask_id, gamma, max_steps, ln_eps, seed, block_index,
-              kind, boost_lo, boost_hi) -> tt_step_desc:
+              kind, boost_lo, boost_hi, sampler: int = SAMPLER_CONFIDENCE,
+              temperature: float = 1.0) -> tt_step_desc:
     return tt_step_desc(attn, H, V, mask_id, float(gamma), max_steps, float(ln_eps),
                         tt_logits_spec(seed & 0xFFFFFFFF, block_index, kind, float(boost_lo),
-                                       float(boost_hi)))
+                                       float(boost_hi)), int(sampler), float(temperature))
 
 
 def step_tensors(**tensors) -> tt_step_tensors:

@@ -61,7 +61,7 @@ typedef enum {
 } tt_status;
 
 /* ABI revision of this header. */
-#define TT_ABI_VERSION 1
+#define TT_ABI_VERSION 2
 TT_API int tt_abi_version(void);
 
 /* Static name of a status code. */
@@ -205,6 +205,48 @@ TT_API tt_status tt_confidence_unmask(const float* logits, int32_t* ids, int32_t
                                size_t workspace_bytes, tt_stream_t stream);
 
 /* --------------------------------------------------------------------------------
+ * Sampler variants of the unmask step
+ *
+ * "Nemotron-Labs-TwoTower" wiki: "Block-wise generation" names, besides confidence
+ * unmasking, the standard predict-and-noise sampler (predict a clean block, re-mask
+ * low-confidence positions by the noise schedule); the model-card example in "Release
+ * history and artifacts" passes a sampling temperature; the opening summary describes
+ * a mock-AR two-tower mode that predicts one token per step.
+ *
+ * In every mode: the confidence of a masked position is the largest probability of
+ * softmax(logits / temperature) with the mask id removed, the token its argmax (ties
+ * to the lowest id, independent of the temperature), decoded positions stay fixed,
+ * and steps[b] advances by one for every sequence that had a masked position.
+ *   TT_SAMPLER_CONFIDENCE: commit every position with confidence >= gamma, and at
+ *     least ceil(m / (T - steps)) of them (the most confident) - tt_confidence_unmask
+ *     is this mode at temperature 1;
+ *   TT_SAMPLER_MOCK_AR: commit exactly one position, the leftmost still masked;
+ *   TT_SAMPLER_PREDICT_NOISE: after the step, floor(S * (T - steps - 1) / T)
+ *     positions stay masked (0 at the last step), the most confident are committed,
+ *     at least one.  Equal confidences go to the lower position.
+ * Arguments, layouts, workspace (tt_confidence_unmask_workspace) and errors are those
+ * of tt_confidence_unmask; `sampler` is a host pointer.
+ * -------------------------------------------------------------------------------- */
+typedef enum {
+    TT_SAMPLER_CONFIDENCE = 0,
+    TT_SAMPLER_MOCK_AR = 1,
+    TT_SAMPLER_PREDICT_NOISE = 2
+} tt_sampler_kind;
+
+typedef struct {
+    int kind;          /* tt_sampler_kind */
+    float gamma;       /* confidence threshold (TT_SAMPLER_CONFIDENCE) */
+    float temperature; /* > 0 */
+    int max_steps;     /* T, 1..255 */
+} tt_sampler;
+
+TT_API tt_status tt_sampler_unmask(const float* logits, int32_t* ids, int32_t* n_masked,
+                                   int32_t* steps, float* conf, uint8_t* commit,
+                                   uint8_t* commit_step, int B, int S, int V, int32_t mask_id,
+                                   const tt_sampler* sampler, void* workspace,
+                                   size_t workspace_bytes, tt_stream_t stream);
+
+/* --------------------------------------------------------------------------------
  * tt_confidence_unmask_noalloc: the same confidence-unmasking step, for callers that
  * cannot provide a workspace.  The pages describing the method have no counterpart
  * to this entry point; it exists for callers whose device memory is owned entirely
@@ -257,6 +299,8 @@ typedef struct {
     int max_steps;          /* T */
     float ln_eps;
     tt_logits_spec logits;
+    int sampler;            /* tt_sampler_kind: TT_SAMPLER_CONFIDENCE (0) for the main sampler */
+    float temperature;      /* > 0; 1 = plain softmax */
 } tt_step_desc;
 
 typedef struct {
