@@ -61,29 +61,39 @@ __device__ __forceinline__ Red warp_combine(Red v, float ts) {
 }
 
 // Folds one batch of values (ids ascending in the order given) into the running
-// triple of this thread.
+// triple of this thread.  The batch maximum comes from a 3-input max tree; its id is
+// looked for only when it beats the running maximum (rare once a row's first batches
+// are in), and an equal maximum keeps the running, lower id.  The exponentials use one
+// packed FMA per pair and a packed running sum.
 template <int N>
 __device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&id)[N], float ts) {
+    static_assert(N % 2 == 0, "pairs");
     float bm = x[0];
-    int ba = id[0];
 #pragma unroll
-    for (int i = 1; i < N; ++i) {
-        if (x[i] > bm) {
-            bm = x[i];
-            ba = id[i];
-        }
-    }
+    for (int i = 1; i + 1 < N; i += 2) bm = ttk::fmax3(bm, x[i], x[i + 1]);
+    if (N % 2 == 0) bm = fmaxf(bm, x[N - 1]);
     if (bm > acc.m) {
+        int ba = id[N - 1];
+#pragma unroll
+        for (int i = N - 1; i >= 0; --i)
+            if (x[i] == bm) ba = id[i];  // the first (lowest) id attaining the maximum
         acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - bm) * ts);
         acc.m = bm;
         acc.a = ba;
     }
     if (acc.m == -CUDART_INF_F) return;
     const float off = -acc.m * ts;
-    float s = 0.f;
+    const uint64_t ts2 = ttk::f2_pack(ts, ts), off2 = ttk::f2_pack(off, off);
+    uint64_t s2 = ttk::f2_pack(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < N; ++i) s += exp2f(fmaf(x[i], ts, off));
-    acc.s += s;
+    for (int i = 0; i < N; i += 2) {
+        float e0, e1;
+        ttk::f2_unpack(ttk::f2_fma(ttk::f2_pack(x[i], x[i + 1]), ts2, off2), e0, e1);
+        s2 = ttk::f2_add(s2, ttk::f2_pack(exp2f(e0), exp2f(e1)));
+    }
+    float s0, s1;
+    ttk::f2_unpack(s2, s0, s1);
+    acc.s += s0 + s1;
 }
 
 // Ticket increment with acquire-release semantics at GPU scope: this thread's earlier
@@ -233,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
             }
         } else {
             for (int v = v0 + tid; v < v1; v += kThreads) {
-                float x[1] = {__ldcs(rowp + v)};
-                int id[1] = {v};
+                float x[2] = {__ldcs(rowp + v), -CUDART_INF_F};
+                int id[2] = {v, 0x7fffffff};
                 if (v == mid) x[0] = -CUDART_INF_F;
-                fold<1>(acc, x, id, p.temp_scale);
+                fold<2>(acc, x, id, p.temp_scale);
             }
         }
         acc = warp_combine(acc, p.temp_scale);
