@@ -14,7 +14,9 @@ Sources ("Nemotron-Labs-TwoTower" wiki page unless stated otherwise):
   tower's layer-i cache followed by the block's own keys, bidirectional in the block);
 * confidence unmasking and the timestep rule - section "Block-wise generation";
 * sampler variants (temperature, mock-AR, predict-and-noise) - sections
-  "Block-wise generation" and "Release history and artifacts" and the opening summary.
+  "Block-wise generation" and "Release history and artifacts" and the opening summary;
+* the outer loop (block append, stopping) - section "Block-wise generation" and the
+  MLX README's "Configuration (diffusion)".
 
 Every function computes the plain definition: no blocking, no fusion, no reordering
 beyond what the definition states.  Readings where the pages are silent are listed
@@ -25,6 +27,7 @@ from .attention import denoise_attention, denoise_attention_rows, context_kv
 from .unmask import row_confidence, unmask_step
 from .loop import denoise_block, denoise_block_batch
 from .samplers import sampler_step, sampler_block, row_confidence_t
+from .outer import append_block, generate
 
 __all__ = [
     "adaln_modulate",
@@ -38,4 +41,6 @@ __all__ = [
     "sampler_step",
     "sampler_block",
     "row_confidence_t",
+    "append_block",
+    "generate",
 ]

@@ -438,3 +438,97 @@ def check_predict_noise_schedule(step_fn):
 SAMPLER_CHECKS = [check_temperature_closed_form, check_temperature_vs_scipy,
                   check_temperature_one_is_plain_confidence, check_mock_ar_left_to_right,
                   check_mock_ar_skips_decoded_positions, check_predict_noise_schedule]
+
+
+# ----------------------------------------------------------------------------------
+# outer loop (Algorithm 1): cache append and stopping
+# ----------------------------------------------------------------------------------
+def _append_case(seed, paged):
+    """A small batch: context lengths 5 / 0 / 9 with room for two more blocks of S=3."""
+    rng = np.random.default_rng(seed)
+    B, S, Hkv, Hq, D = 3, 3, 2, 4, 8
+    lens = np.array([5, 0, 9])
+    w = synth.Workload("tiny", B=B, L=int(lens.max()), S=S, Hq=Hq, Hkv=Hkv, D=D, H=8, V=16,
+                       paged=False)
+    base = synth.make_attention_inputs(w, seed, ctx_len=lens.astype(np.int32))
+    cap = int(lens.max()) + 2 * S
+    kc = np.zeros((B, cap, Hkv, D), np.uint16)
+    vc = np.zeros((B, cap, Hkv, D), np.uint16)
+    for b in range(B):
+        kc[b, :lens[b]] = base["k_ctx"][b, :lens[b]]
+        vc[b, :lens[b]] = base["v_ctx"][b, :lens[b]]
+    if not paged:
+        return dict(k_ctx=kc, v_ctx=vc), base, lens, cap
+    # the same logical rows in shuffled 64-row pages
+    n_pages = B * ((cap + 63) // 64)
+    perm = rng.permutation(n_pages)
+    pt = perm.reshape(B, -1).astype(np.int64)
+    kp = np.zeros((n_pages, 64, Hkv, D), np.uint16)
+    vp = np.zeros((n_pages, 64, Hkv, D), np.uint16)
+    for b in range(B):
+        for t in range(cap):
+            kp[pt[b, t // 64], t % 64] = kc[b, t]
+            vp[pt[b, t // 64], t % 64] = vc[b, t]
+    return dict(k_pages=kp, v_pages=vp, page_table=pt), base, lens, cap
+
+
+def check_append_then_attend_equals_concatenation(append_fn):
+    """Two blocks appended, then a third block attends: torch SDPA over the explicitly
+    concatenated keys [context ; block 0 ; block 1 ; own block] must agree."""
+    for paged in (False, True):
+        cache, base, lens, cap = _append_case(7 + paged, paged)
+        B, S, Hkv, D = base["k_blk"].shape
+        rng = np.random.default_rng(3)
+        blks = [synth.f32_to_bf16_bits(rng.standard_normal((2, B, S, Hkv, D)).astype(np.float32))
+                for _ in range(2)]
+        ctx, gen, done = lens.copy(), np.zeros(B, np.int64), np.zeros(B, np.uint8)
+        for kb_vb in blks:
+            ids = np.full((B, S), 11)
+            r = append_fn(cache, kb_vb[0], kb_vb[1], ctx, ids, 99, 1000, gen, done)
+            cache = {k: r[k] for k in cache}
+            ctx, gen, done = r["ctx_len"], r["generated"], r["done"]
+        assert ctx.tolist() == (lens + 2 * S).tolist()
+        # attention of the current block over the appended cache
+        inp = dict(q=base["q"], k_blk=base["k_blk"], v_blk=base["v_blk"], ctx_len=ctx.astype(np.int32))
+        if paged:
+            inp.update(k_pages=cache["k_pages"], v_pages=cache["v_pages"], page_table=cache["page_table"])
+        else:
+            inp.update(k_ctx=cache["k_ctx"], v_ctx=cache["v_ctx"])
+        # explicit concatenation, contiguous
+        L = int(ctx.max())
+        kc = np.zeros((B, L, Hkv, D), np.uint16)
+        vc = np.zeros((B, L, Hkv, D), np.uint16)
+        for b in range(B):
+            n = int(lens[b])
+            kc[b, :n] = base["k_ctx"][b, :n]
+            vc[b, :n] = base["v_ctx"][b, :n]
+            for i, kb_vb in enumerate(blks):
+                kc[b, n + i * S:n + (i + 1) * S] = kb_vb[0][b]
+                vc[b, n + i * S:n + (i + 1) * S] = kb_vb[1][b]
+        ref = dict(q=base["q"], k_blk=base["k_blk"], v_blk=base["v_blk"], ctx_len=ctx.astype(np.int32),
+                   k_ctx=kc, v_ctx=vc)
+        want, _ = torch_reference(ref, 0.35)
+        import oracle
+        got, _ = oracle.denoise_attention(inp, 0.35)
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+
+
+def check_append_stops(append_fn):
+    cache, base, lens, cap = _append_case(11, False)
+    B, S = base["k_blk"].shape[:2]
+    ids = np.array([[1, 2, 3], [4, 99, 6], [7, 8, 9]])  # sequence 1 commits the EOS id 99
+    gen0 = np.array([0, 0, 3])  # sequence 2 reaches max_new = 6 exactly
+    done0 = np.array([0, 0, 0], np.uint8)
+    r = append_fn(cache, base["k_blk"], base["v_blk"], lens, ids, 99, 6, gen0, done0)
+    assert r["done"].tolist() == [0, 1, 1]          # EOS; 3 + 3 reaches 6
+    assert r["generated"].tolist() == [3, 3, 6]
+    assert r["ctx_len"].tolist() == (lens + S).tolist()
+    # a done sequence is left alone: no rows written, ctx_len and generated unchanged
+    r2 = append_fn({k: r[k] for k in cache}, base["k_blk"], base["v_blk"], r["ctx_len"], ids, 99, 100,
+                   r["generated"], r["done"])
+    assert r2["ctx_len"].tolist() == [lens[0] + 2 * S, lens[1] + S, lens[2] + S]
+    assert np.array_equal(r2["k_ctx"][1], r["k_ctx"][1]) and np.array_equal(r2["k_ctx"][2], r["k_ctx"][2])
+    assert r2["generated"].tolist() == [6, 3, 6]
+
+
+OUTER_CHECKS = [check_append_then_attend_equals_concatenation, check_append_stops]
