@@ -794,4 +794,81 @@ tt_status tt_denoise_block_loop(const tt_step_desc* desc, const tt_step_tensors*
     return TT_OK;
 }
 
+tt_status tt_append_block(const tt_attn_dims* dims, const void* k_blk, const void* v_blk,
+                          void* k_ctx, void* v_ctx, const int32_t* page_table, int32_t* ctx_len,
+                          const int32_t* ids, const tt_stop_spec* stop, int32_t* generated,
+                          uint8_t* done, int32_t* out_tokens, int out_stride, int out_offset,
+                          tt_stream_t stream) {
+    tti::AttnGeom g;
+    TT_TRY(check_attn(dims, g));
+    if (stop == nullptr) return fail(TT_ERR_INVALID_ARG, "stop is null");
+    TT_TRY(need_ptr(k_blk, "k_blk"));
+    TT_TRY(need_ptr(v_blk, "v_blk"));
+    TT_TRY(need_ptr(k_ctx, "k_ctx"));
+    TT_TRY(need_ptr(v_ctx, "v_ctx"));
+    TT_TRY(need_ptr(ctx_len, "ctx_len", false));
+    TT_TRY(need_ptr(ids, "ids", false));
+    TT_TRY(need_ptr(generated, "generated", false));
+    TT_TRY(need_ptr(done, "done", false));
+    if (g.page_size) TT_TRY(need_ptr(page_table, "page_table", false));
+    else if (g.max_ctx < g.S) return fail(TT_ERR_INVALID_ARG, "a contiguous cache needs max_ctx >= S");
+    if (out_tokens != nullptr && (out_offset < 0 || out_stride < out_offset + g.S))
+        return fail(TT_ERR_INVALID_ARG, "out_tokens must hold S tokens at out_offset");
+    int* err = nullptr;
+    TT_TRY(device_err_word(&err));
+    tti::AppendParams p;
+    p.k_blk = static_cast<const uint16_t*>(k_blk);
+    p.v_blk = static_cast<const uint16_t*>(v_blk);
+    p.k_ctx = static_cast<uint16_t*>(k_ctx);
+    p.v_ctx = static_cast<uint16_t*>(v_ctx);
+    p.page_table = g.page_size ? page_table : nullptr;
+    p.ctx_len = ctx_len;
+    p.ids = ids;
+    p.generated = generated;
+    p.done = done;
+    p.out_tokens = out_tokens;
+    p.out_stride = out_stride;
+    p.out_offset = out_offset;
+    p.B = g.B;
+    p.S = g.S;
+    p.Hkv = g.Hkv;
+    p.D = g.D;
+    p.capacity = g.page_size ? 0 : g.max_ctx;
+    p.page_size = g.page_size;
+    p.max_pages = g.max_pages;
+    p.num_pages = g.num_pages;
+    p.eos_id = stop->eos_id;
+    p.pad_id = stop->pad_id;
+    p.max_new_tokens = stop->max_new_tokens;
+    p.err = err;
+    TT_CUDA(tti::launch_append_block(p, reinterpret_cast<cudaStream_t>(stream)));
+    return TT_OK;
+}
+
+tt_status tt_generate(const tt_step_desc* desc, const tt_step_tensors* t, int n_blocks,
+                      const tt_stop_spec* stop, int32_t* generated, uint8_t* done,
+                      int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                      tt_stream_t stream) {
+    if (desc == nullptr || t == nullptr || stop == nullptr)
+        return fail(TT_ERR_INVALID_ARG, "desc, tensors and stop must be given");
+    if (n_blocks < 1) return fail(TT_ERR_INVALID_ARG, "n_blocks must be >= 1");
+    if ((long long)n_blocks * desc->attn.S > 0x7fffffffLL) return fail(TT_ERR_INVALID_ARG, "n_blocks too large");
+    TT_TRY(need_ptr(t->ctx_len, "ctx_len (in/out here)", false));
+    TT_TRY(need_ptr(out_tokens, "out_tokens", false));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int B = desc->attn.B, S = desc->attn.S;
+    for (int k = 0; k < n_blocks; ++k) {
+        TT_CUDA(tti::launch_block_start(t->ids, t->steps, t->commit_step, done, B, S, desc->mask_id,
+                                        stop->pad_id, st));
+        tt_step_desc dk = *desc;
+        dk.logits.block_index = desc->logits.block_index + k;
+        TT_TRY(tt_denoise_block_loop(&dk, t, workspace, workspace_bytes, stream));
+        TT_TRY(tt_append_block(&desc->attn, t->k_blk, t->v_blk, const_cast<void*>(t->k_ctx),
+                               const_cast<void*>(t->v_ctx), t->page_table,
+                               const_cast<int32_t*>(t->ctx_len), t->ids, stop, generated, done,
+                               out_tokens, n_blocks * S, k * S, stream));
+    }
+    return TT_OK;
+}
+
 }  // extern "C"

@@ -157,6 +157,30 @@ struct AttnMergeParams {
 };
 cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream);
 
+// ----------------------------------------------------------------------- outer loop
+struct AppendParams {
+    const uint16_t* k_blk;   // bf16 [B][S][Hkv][D]
+    const uint16_t* v_blk;
+    uint16_t* k_ctx;         // contiguous [B][capacity][Hkv][D] or pages [P][64][Hkv][D]
+    uint16_t* v_ctx;
+    const int32_t* page_table;  // [B][max_pages] or null
+    int32_t* ctx_len;        // [B] in/out
+    const int32_t* ids;      // [B][S] the committed block
+    int32_t* generated;      // [B] in/out
+    uint8_t* done;           // [B] in/out
+    int32_t* out_tokens;     // [B][out_stride] or null: this block at out_offset
+    int out_stride, out_offset;
+    int B, S, Hkv, D;
+    int capacity;            // contiguous: rows per sequence
+    int page_size, max_pages, num_pages;
+    int32_t eos_id, pad_id;
+    int max_new_tokens;
+    int* err;
+};
+cudaError_t launch_append_block(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_block_start(int32_t* ids, int32_t* steps, uint8_t* commit_step, const uint8_t* done,
+                               int B, int S, int32_t mask_id, int32_t pad_id, cudaStream_t stream);
+
 // ------------------------------------------------------------------------------ loop
 struct InitParams {
     const int32_t* ids;

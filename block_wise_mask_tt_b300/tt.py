@@ -60,6 +60,10 @@ class tt_step_desc(ctypes.Structure):
 SAMPLER_CONFIDENCE, SAMPLER_MOCK_AR, SAMPLER_PREDICT_NOISE = 0, 1, 2
 
 
+class tt_stop_spec(ctypes.Structure):
+    _fields_ = [("eos_id", ctypes.c_int32), ("pad_id", ctypes.c_int32), ("max_new_tokens", ctypes.c_int)]
+
+
 class tt_sampler(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("gamma", ctypes.c_float), ("temperature", ctypes.c_float),
                 ("max_steps", ctypes.c_int)]
@@ -95,6 +99,10 @@ _SIGS = {
     "tt_confidence_unmask_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
                                           ctypes.c_float, _I, _P]),
     "tt_denoise_workspace": (ctypes.c_size_t, [ctypes.POINTER(tt_step_desc)]),
+    "tt_append_block": (_I, [ctypes.POINTER(tt_attn_dims), _P, _P, _P, _P, _P, _P, _P,
+                             ctypes.POINTER(tt_stop_spec), _P, _P, _P, _I, _I, _P]),
+    "tt_generate": (_I, [ctypes.POINTER(tt_step_desc), ctypes.POINTER(tt_step_tensors), _I,
+                         ctypes.POINTER(tt_stop_spec), _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "tt_denoise_step": (_I, [ctypes.POINTER(tt_step_desc), ctypes.POINTER(tt_step_tensors), _P,
                              ctypes.c_size_t, _P]),
     "tt_denoise_block_loop": (_I, [ctypes.POINTER(tt_step_desc), ctypes.POINTER(tt_step_tensors),
@@ -273,3 +281,23 @@ def tt_denoise_step(desc: tt_step_desc, tensors: tt_step_tensors, ws, stream=Non
 def tt_denoise_block_loop(desc: tt_step_desc, tensors: tt_step_tensors, ws, stream=None) -> None:
     _check(lib.tt_denoise_block_loop(ctypes.byref(desc), ctypes.byref(tensors), ws.data_ptr(),
                                      ws.numel(), _stream(stream)))
+
+
+def tt_append_block(dims: tt_attn_dims, k_blk, v_blk, k_ctx, v_ctx, page_table, ctx_len, ids,
+                    stop: tt_stop_spec, generated, done, out_tokens=None, out_stride=0, out_offset=0,
+                    stream=None) -> None:
+    _check(lib.tt_append_block(
+        ctypes.byref(dims), _ptr(k_blk, "k_blk", _BF16), _ptr(v_blk, "v_blk", _BF16),
+        _ptr(k_ctx, "k_ctx", _BF16), _ptr(v_ctx, "v_ctx", _BF16), _ptr(page_table, "page_table", _I32),
+        _ptr(ctx_len, "ctx_len", _I32, dims.B), _ptr(ids, "ids", _I32, dims.B * dims.S),
+        ctypes.byref(stop), _ptr(generated, "generated", _I32, dims.B), _ptr(done, "done", _U8, dims.B),
+        _ptr(out_tokens, "out_tokens", _I32), int(out_stride), int(out_offset), _stream(stream)))
+
+
+def tt_generate(desc: tt_step_desc, tensors: tt_step_tensors, n_blocks: int, stop: tt_stop_spec,
+                generated, done, out_tokens, ws, stream=None) -> None:
+    B, S = desc.attn.B, desc.attn.S
+    _check(lib.tt_generate(ctypes.byref(desc), ctypes.byref(tensors), int(n_blocks), ctypes.byref(stop),
+                           _ptr(generated, "generated", _I32, B), _ptr(done, "done", _U8, B),
+                           _ptr(out_tokens, "out_tokens", _I32, B * n_blocks * S), ws.data_ptr(),
+                           ws.numel(), _stream(stream)))

@@ -346,6 +346,49 @@ TT_API tt_status tt_denoise_block_loop(const tt_step_desc* desc, const tt_step_t
                                 void* workspace, size_t workspace_bytes,
                                 tt_stream_t stream);
 
+/* --------------------------------------------------------------------------------
+ * Algorithm 1, the block-wise outer loop
+ *
+ * "Nemotron-Labs-TwoTower" wiki, "Block-wise generation": once a block is clean it is
+ * committed, the context tower processes the committed tokens causally to update its
+ * caches, and the loop continues with the next block.  The MLX README
+ * ("Configuration (diffusion)") adds the stopping knobs: a number of new tokens and an
+ * end-of-sequence id.  The context tower's forward needs trained weights: the
+ * keys/values appended for a committed block are that block's own k_blk / v_blk.
+ * -------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t eos_id;          /* a block that commits it ends the sequence (-1: none)  */
+    int32_t pad_id;          /* fills the positions of finished sequences            */
+    int max_new_tokens;      /* a sequence ends once it has generated this many      */
+} tt_stop_spec;
+
+/* For every sequence b with done[b] == 0: copies k_blk[b] / v_blk[b] (S rows each) to
+ * logical positions ctx_len[b] .. ctx_len[b] + S - 1 of its cache (dims->max_ctx rows
+ * per sequence for a contiguous cache, which must fit them; page_table pages for a
+ * paged one, which must exist), then ctx_len[b] += S, generated[b] += S, and done[b]
+ * = 1 if ids[b] holds stop->eos_id or generated[b] >= stop->max_new_tokens.  A
+ * sequence whose rows do not fit is skipped and the device error word set.
+ * out_tokens (nullable, int32 [B][out_stride]) receives ids[b] at out_offset, or the
+ * pad id for a sequence that was already done.  All pointers are device pointers except
+ * dims and stop. */
+TT_API tt_status tt_append_block(const tt_attn_dims* dims, const void* k_blk, const void* v_blk,
+                                 void* k_ctx, void* v_ctx, const int32_t* page_table,
+                                 int32_t* ctx_len, const int32_t* ids, const tt_stop_spec* stop,
+                                 int32_t* generated, uint8_t* done, int32_t* out_tokens,
+                                 int out_stride, int out_offset, tt_stream_t stream);
+
+/* n_blocks iterations of the outer loop from the current caches: for block k, every
+ * running sequence starts fully masked (finished ones hold the pad id), the block is
+ * decoded exactly as tt_denoise_block_loop does with logits block index
+ * desc->logits.block_index + k, and tt_append_block then appends it (out_offset =
+ * k * S).  t->k_ctx, t->v_ctx and t->ctx_len are updated in place (they are in/out
+ * here), as are generated and done.  out_tokens: int32 [B][n_blocks * S].  Same
+ * workspace as tt_denoise_block_loop; one asynchronous sequence of launches. */
+TT_API tt_status tt_generate(const tt_step_desc* desc, const tt_step_tensors* t, int n_blocks,
+                             const tt_stop_spec* stop, int32_t* generated, uint8_t* done,
+                             int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                             tt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

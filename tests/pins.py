@@ -443,10 +443,10 @@ SAMPLER_CHECKS = [check_temperature_closed_form, check_temperature_vs_scipy,
 # ----------------------------------------------------------------------------------
 # outer loop (Algorithm 1): cache append and stopping
 # ----------------------------------------------------------------------------------
-def _append_case(seed, paged):
+def _append_case(seed, paged, D=8):
     """A small batch: context lengths 5 / 0 / 9 with room for two more blocks of S=3."""
     rng = np.random.default_rng(seed)
-    B, S, Hkv, Hq, D = 3, 3, 2, 4, 8
+    B, S, Hkv, Hq = 3, 3, 2, 4
     lens = np.array([5, 0, 9])
     w = synth.Workload("tiny", B=B, L=int(lens.max()), S=S, Hq=Hq, Hkv=Hkv, D=D, H=8, V=16,
                        paged=False)
