@@ -63,6 +63,9 @@ def parse_args():
                     help="profiling aid: run only --reps standalone calls of one entry point on "
                          "the workload (after 3 untimed ones) and print their mean time")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--generate", type=int, default=32,
+                    help="also time tt_generate over this many blocks (Algorithm 1's outer loop: "
+                         "decode, append the block to the cache, next block); 0 skips it")
     return ap.parse_args()
 
 
@@ -96,10 +99,10 @@ def job_throughput(steps_per_rank: int, world: int, elapsed_max_s: float) -> flo
 # summarised under profiles/ (denoise_step_*.md: cold-cache, per launch).  Missing
 # entries are reported as null.
 NCU_TRAFFIC = {
-    ("c1_single_B1_L4096_S16_32q2kv_D128", "attn"): 4.47e6 + 4.28e6,
-    ("c1_single_B1_L4096_S16_32q2kv_D128", "unmask"): 8.42e6,
-    ("c2_batched_B32_L8192_S16_32q2kv_D128", "attn"): 274.55e6 + 1.76e6 + 17.06e6,
-    ("c2_batched_B32_L8192_S16_32q2kv_D128", "unmask"): 268.49e6 + 0.12e6,
+    ("c1_single_B1_L4096_S16_32q2kv_D128", "attn"): 4.41e6 + 4.28e6,
+    ("c1_single_B1_L4096_S16_32q2kv_D128", "unmask"): 8.43e6,
+    ("c2_batched_B32_L8192_S16_32q2kv_D128", "attn"): 273.23e6 + 0.09e6 + 17.06e6,
+    ("c2_batched_B32_L8192_S16_32q2kv_D128", "unmask"): 268.49e6 + 0.11e6,
 }
 
 
@@ -423,6 +426,77 @@ def run_e2e(wb: Workbench, plan, torch, tt):
     return s.elapsed_time(e) / 1e3, h2d, d2h
 
 
+def run_generate(wb: Workbench, n_blocks: int, flush, reps: int = 3):
+    """Algorithm 1's outer loop on the device: the prompt cache of the workload with room
+    for n_blocks more blocks, then tt_generate (per block: reset, the captured denoise
+    loop, tt_append_block) with no end-of-sequence id, so every sequence decodes every
+    block.  Returns a dict for the JSON line (best of reps, L2 flushed before each)."""
+    tt, torch, w = wb.tt, wb.torch, wb.w
+    B, S = w.B, w.S
+    L0 = wb.t["k_ctx"].shape[1]
+    cap = L0 + n_blocks * S
+    kc = torch.zeros((B, cap, w.Hkv, w.D), dtype=torch.int16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kc[:, :L0].copy_(wb.t["k_ctx"])
+    vc[:, :L0].copy_(wb.t["v_ctx"])
+    ctx0 = wb.t["ctx_len"].clone()
+    dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, cap, 0, 0, 0, w.softmax_scale, 0)
+    desc = tt.step_desc(dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps, wb.seed, 0,
+                        w.logits_kind, w.boost_lo, w.boost_hi, sampler=wb.desc.sampler,
+                        temperature=wb.desc.temperature)
+    t = dict(wb.t)
+    t.update(k_ctx=kc, v_ctx=vc, ctx_len=ctx0.clone())
+    ts = tt.step_tensors(**t)
+    ws = tt.workspace(tt.tt_denoise_workspace(desc))
+    gen = torch.zeros(B, dtype=torch.int32, device="cuda")
+    done = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, n_blocks * S), dtype=torch.int32, device="cuda")
+    stop = tt.tt_stop_spec(-1, 0, n_blocks * S)
+
+    def reset():
+        t["ctx_len"].copy_(ctx0)
+        gen.zero_()
+        done.zero_()
+
+    best = None
+    for _ in range(reps + 1):  # the first call captures the block-loop graph: untimed
+        flush()
+        reset()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        tt.tt_generate(desc, ts, n_blocks, stop, gen, done, out, ws)
+        e.record()
+        e.synchronize()
+        dt = s.elapsed_time(e) / 1e3
+        best = dt if best is None or dt < best else best
+    if tt.tt_device_status(True) != 0:
+        raise RuntimeError("device-side error reported by tt_generate")
+    if t["ctx_len"].tolist() != (ctx0 + n_blocks * S).tolist() or gen.tolist() != [n_blocks * S] * B:
+        raise RuntimeError("tt_generate did not decode every block")
+    # the append kernel alone (one block into the grown cache, state reset between calls)
+    ctx_mid = ctx0 + (n_blocks - 1) * S
+    ta = []
+    for _ in range(reps + 2):
+        t["ctx_len"].copy_(ctx_mid)
+        done.zero_()
+        flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        tt.tt_append_block(dims, t["k_blk"], t["v_blk"], kc, vc, None, t["ctx_len"], t["ids"], stop, gen,
+                           done, out, n_blocks * S, 0)
+        e.record()
+        e.synchronize()
+        ta.append(s.elapsed_time(e) / 1e3)
+    ta = sorted(ta[2:])[len(ta[2:]) // 2]
+    append_bytes = 2 * 2 * B * S * w.Hkv * w.D * 2  # K and V rows, read once and written once
+    return {"blocks": n_blocks, "tokens": B * S * n_blocks, "ms": best * 1e3,
+            "tokens_per_s": B * S * n_blocks / best, "blocks_per_s": n_blocks / best,
+            "cache_rows_start": int(ctx0.max().item()), "eos": "none (every block decoded)",
+            "append_block_us": ta * 1e6, "append_block_bytes": append_bytes,
+            "append_block_GB_s": append_bytes / ta / 1e9,
+            "l2": "flushed before each timed call"}
+
+
 # ------------------------------------------------------------------ CPU oracle legs
 def oracle_block_time(w: synth.Workload, seed: int, block: int, max_steps=None, b_sample=None):
     """The oracle decoding one block of the workload on the host cores.
@@ -610,6 +684,10 @@ def main():
                "h2d_bytes_per_step": int(h2d * len(plan) / total_steps),
                "d2h_bytes_per_step": int(d2h * len(plan) / total_steps)}
 
+    gen_line = None
+    if args.generate > 0 and not w.paged:
+        gen_line = run_generate(wb, args.generate, flush)
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -638,6 +716,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "generate": gen_line,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
