@@ -183,6 +183,7 @@ class Workload:
     blocks: int = 1
     qkv_std: float = 1.0
     mod_std: float = 0.1
+    lm_logit_std: float = 10.0  # spread of the LM head's logits for unit-RMS hidden rows
 
     @property
     def G(self) -> int:
@@ -296,3 +297,22 @@ def make_adaln_inputs(w: Workload, seed: int = 0) -> dict:
         "scale_table": (_rng(seed, 25).standard_normal((S + 1, H), dtype=np.float32)
                         * np.float32(w.mod_std)),
     }
+
+
+def make_hidden(w: Workload, seed: int = 0) -> np.ndarray:
+    """bf16 hidden rows [B][S][H], N(0, 1): the input of the LM head in standalone calls."""
+    return _normal_bf16(_rng(seed, 30), (w.B, w.S, w.H), 1.0, 1.0)
+
+
+def make_lmhead_weights(w: Workload, seed: int = 0, rows: int = 8192) -> np.ndarray:
+    """bf16 vocabulary projection [V][H] (one row per token id), N(0, sigma^2) with
+    sigma = lm_logit_std / sqrt(H), so unit-RMS hidden rows give logits of standard
+    deviation lm_logit_std.  Drawn in blocks of rows to bound host memory."""
+    V, H = w.V, w.H
+    out = np.empty((V, H), dtype=np.uint16)
+    r = _rng(seed, 31)
+    sigma = w.lm_logit_std / math.sqrt(H)
+    for v0 in range(0, V, rows):
+        v1 = min(V, v0 + rows)
+        out[v0:v1] = _normal_bf16(r, (v1 - v0, H), sigma, 1.0)
+    return out

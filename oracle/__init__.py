@@ -16,7 +16,8 @@ Sources ("Nemotron-Labs-TwoTower" wiki page unless stated otherwise):
 * sampler variants (temperature, mock-AR, predict-and-noise) - sections
   "Block-wise generation" and "Release history and artifacts" and the opening summary;
 * the outer loop (block append, stopping) - section "Block-wise generation" and the
-  MLX README's "Configuration (diffusion)".
+  MLX README's "Configuration (diffusion)";
+* the LM head that feeds the unmask step - section "Block-wise generation".
 
 Every function computes the plain definition: no blocking, no fusion, no reordering
 beyond what the definition states.  Readings where the pages are silent are listed
@@ -28,6 +29,7 @@ from .unmask import row_confidence, unmask_step
 from .loop import denoise_block, denoise_block_batch
 from .samplers import sampler_step, sampler_block, row_confidence_t
 from .outer import append_block, generate
+from .lmhead import lm_head_logits, lm_head_step
 
 __all__ = [
     "adaln_modulate",
@@ -43,4 +45,6 @@ __all__ = [
     "row_confidence_t",
     "append_block",
     "generate",
+    "lm_head_logits",
+    "lm_head_step",
 ]

@@ -532,3 +532,96 @@ def check_append_stops(append_fn):
 
 
 OUTER_CHECKS = [check_append_then_attend_equals_concatenation, check_append_stops]
+
+
+# ----------------------------------------------------------------------------------
+# LM head feeding the unmask step
+# ----------------------------------------------------------------------------------
+BF16_ONE = 0x3F80
+
+
+def _rand_bf16(seed, shape, std=1.0):
+    rng = np.random.default_rng(seed)
+    return synth.f32_to_bf16_bits((rng.standard_normal(shape) * std).astype(np.float32))
+
+
+def check_lm_head_one_hot_rows(logits_fn):
+    """W[j] = e_{pi(j)} (exact ones): logit[r][j] is the hidden component pi(j), exactly."""
+    V, H = 40, 24
+    pi = np.random.default_rng(1).integers(0, H, V)
+    W = np.zeros((V, H), np.uint16)
+    W[np.arange(V), pi] = BF16_ONE
+    h = _rand_bf16(2, (5, H))
+    got = logits_fn(h, W)
+    assert got.shape == (5, V)
+    want = synth.bf16_bits_to_f32(h).astype(np.float64)[:, pi]
+    assert np.array_equal(got, want)
+
+
+def check_lm_head_vs_torch_linear(logits_fn):
+    h = _rand_bf16(3, (5, 96))
+    W = _rand_bf16(4, (70, 96), 0.3)
+    want = F.linear(_bf(h), _bf(W)).numpy()
+    np.testing.assert_allclose(logits_fn(h, W), want, rtol=1e-12, atol=1e-12)
+
+
+def check_lm_head_scaled_basis_rows(step_fn):
+    """h[s] = a_s e_{k_s}: logit[j] = a_s W[j][k_s]; token and confidence follow from
+    column k_s of W alone (closed form written out with loops)."""
+    V = H = 48
+    mask = 5
+    W = _rand_bf16(6, (V, H))
+    Wf = synth.bf16_bits_to_f32(W).astype(np.float64)
+    S = 6
+    ks = [0, 7, 7, 19, 33, 47]
+    amps = [0.5, 1.0, 2.0, 3.0, 1.5, 4.0]
+    h = np.zeros((S, H), np.uint16)
+    for s in range(S):
+        h[s, ks[s]] = synth.f32_to_bf16_bits(np.array([amps[s]], np.float32))[0]
+    r = step_fn(h, W, np.full(S, mask), 0, mask, 16, 0, 2.0, 1.0, None)
+    for s in range(S):
+        best, tok = -math.inf, -1
+        for j in range(V):
+            if j != mask and amps[s] * Wf[j, ks[s]] > best:
+                best, tok = amps[s] * Wf[j, ks[s]], j
+        den = 0.0
+        for j in range(V):
+            if j != mask:
+                den += math.exp(amps[s] * Wf[j, ks[s]] - best)
+        assert r["tok"][s] == tok
+        assert abs(r["conf"][s] - 1.0 / den) <= 1e-12
+
+
+def check_lm_head_mask_row_never_emitted(step_fn):
+    """The mask id's row of W is aligned with every hidden row (largest logit): it is
+    neither emitted nor counted in the confidence."""
+    V, H, mask, S = 32, 16, 3, 4
+    W = _rand_bf16(8, (V, H), 0.1)
+    h = _rand_bf16(9, (S, H))
+    W[mask] = synth.f32_to_bf16_bits(np.sign(synth.bf16_bits_to_f32(h).sum(0)).astype(np.float32) * 8)
+    r = step_fn(h, W, np.full(S, mask), 0, mask, S, 0, 0.0, 1.0, None)
+    assert np.all(r["ids"] != mask)
+    lg = synth.bf16_bits_to_f32(h).astype(np.float64) @ synth.bf16_bits_to_f32(W).astype(np.float64).T
+    lg[:, mask] = -np.inf
+    from scipy.special import softmax
+    for s in range(S):
+        assert abs(r["conf"][s] - softmax(lg[s]).max()) <= 1e-12
+
+
+def check_lm_head_decoded_rows_unused(step_fn):
+    """Hidden rows of decoded positions are never read: NaN there changes nothing."""
+    V, H, mask, S = 64, 32, 3, 6
+    W = _rand_bf16(10, (V, H), 0.4)
+    h = _rand_bf16(11, (S, H))
+    ids = np.array([mask, 17, mask, mask, 40, mask])
+    a = step_fn(h, W, ids, 1, mask, S, 0, 0.8, 1.0, None)
+    h2 = h.copy()
+    h2[[1, 4]] = 0x7FC0  # bf16 NaN
+    b = step_fn(h2, W, ids, 1, mask, S, 0, 0.8, 1.0, None)
+    assert np.array_equal(a["ids"], b["ids"]) and np.array_equal(a["conf"], b["conf"])
+    assert np.all(np.isfinite(b["conf"]))
+
+
+LMHEAD_LOGIT_CHECKS = [check_lm_head_one_hot_rows, check_lm_head_vs_torch_linear]
+LMHEAD_STEP_CHECKS = [check_lm_head_scaled_basis_rows, check_lm_head_mask_row_never_emitted,
+                      check_lm_head_decoded_rows_unused]
