@@ -1,0 +1,371 @@
+// LM head fused with confidence unmasking: the logits of the masked positions are
+// formed on the tensor cores and reduced on the fly, so they never reach memory.
+//
+// "Nemotron-Labs-TwoTower" wiki, "Block-wise generation": every step predicts all
+// masked positions of the block (the LM head over their hidden rows), then commits
+// the confident ones.  logit[r][j] = sum_k h[r][k] * W[j][k] with W [V][H] (one row
+// per token id), bf16 operands, fp32 accumulation.
+//
+// Three kernels, chained with programmatic dependent launch:
+//  1. lmhead_gather_kernel: every CTA scans ids (B*S <= 4096) for the masked rows and
+//     their compact order; its warps copy their rows' hidden vectors to the compact
+//     matrix a_c, and CTA 0 publishes dest[] and the row count.
+//  2. lmhead_gemm_kernel: one persistent CTA per SM.  A work item is (128-row tile of
+//     a_c, vocabulary chunk); the chunks split the vocabulary in 64-id units so that
+//     items = row tiles x chunks covers the CTAs once.  Per 256-id vocabulary tile:
+//     warp 0 streams the A tile (128 rows x 64 of H) and four 64-row boxes of W per
+//     64-wide slice of H into a four-stage ring (TMA, 128-byte swizzle); warp 1 issues
+//     tcgen05.mma 128 x 256 x 16 into one of two TMEM accumulators (256 columns each,
+//     so the epilogue of one tile overlaps the products of the next); warps 2-5 (one
+//     TMEM lane = one row per thread) read the accumulator and fold it into the row's
+//     running (max, sum of 2^((x - max) * log2(e) / tau), lowest argmax), with the
+//     mask id and ids past the chunk masked out.  Each item ends with one 16-byte
+//     partial per row.
+//  3. lmhead_finish_kernel: one warp per sequence merges its masked rows' chunk
+//     partials and takes the sampler's commit/remask decision in place (the same
+//     decision code as the unmask kernel).
+// Every wait on an mbarrier is bounded; one that runs out sets the error word, the
+// roles drain what they issued, and TMEM is released.
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "tt_device.cuh"
+#include "tt_internal.h"
+#include "unmask_common.cuh"
+
+namespace tti {
+namespace {
+
+using namespace um;
+
+constexpr int kStages = 4;
+constexpr uint32_t kATile = 128 * 128;                  // 128 rows x 64 bf16
+constexpr uint32_t kBBox = 64 * 128;                    // 64 vocabulary rows x 64 bf16
+constexpr uint32_t kBTile = 4 * kBBox;                  // 256 vocabulary rows
+constexpr uint32_t kStage = kATile + kBTile;            // 48 KiB
+constexpr uint32_t kBarOff = kStages * kStage;          // barriers after the ring
+constexpr uint32_t kSlotOff = kBarOff + 128;            // TMEM address slot
+constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;   // + slack for 1024-B alignment
+constexpr int kGemmThreads = 192;                       // producer, MMA, 4 epilogue warps
+constexpr uint32_t kIdesc = ttk::idesc_bf16(128, 256, false, false);
+constexpr int kGatherRows = 8;                          // rows copied per gather CTA (one per warp)
+
+// Work split shared by the GEMM and the finish kernel.
+struct Plan {
+    int n_mt;      // 128-row tiles of the compact matrix
+    int units;     // 64-id vocabulary units
+    int n_chunks;  // vocabulary chunks per row tile
+};
+__device__ __forceinline__ Plan make_plan(int n_rows, int V, int n_ctas) {
+    Plan pl;
+    pl.n_mt = (n_rows + 127) / 128;
+    pl.units = (V + 63) / 64;
+    pl.n_chunks = pl.n_mt ? max(1, min(pl.units, n_ctas / pl.n_mt)) : 0;
+    return pl;
+}
+
+__global__ void __launch_bounds__(256) lmhead_gather_kernel(LmHeadParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
+    __shared__ int sdest[kLmHeadMaxRows];
+    __shared__ int wsum[8];
+    const int n = p.rows, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t* ids = p.um.ids;
+    const int mask = p.um.mask_id;
+    // thread t owns rows [t * per, (t + 1) * per): count, block-wide exclusive scan, write
+    const int per = (n + 255) / 256;
+    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+    int cnt = 0;
+    for (int i = i0; i < i1; ++i) cnt += (__ldcg(ids + i) == mask) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int base = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        base += (w < warp) ? wsum[w] : 0;
+        total += wsum[w];
+    }
+    int run = base + incl - cnt;
+    for (int i = i0; i < i1; ++i) {
+        const bool m = __ldcg(ids + i) == mask;
+        sdest[i] = m ? run : -1;
+        run += m ? 1 : 0;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int i = tid; i < n; i += 256) p.dest[i] = sdest[i];
+        if (tid == 0) *p.n_rows = total;
+    }
+    const int row = blockIdx.x * kGatherRows + warp;
+    if (warp < kGatherRows && row < n && sdest[row] >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.h + (size_t)row * p.H);
+        uint4* dst = reinterpret_cast<uint4*>(p.a_c + (size_t)sdest[row] * p.H);
+        for (int c = lane; c < p.H / 8; c += 32) dst[c] = __ldcg(src + c);
+    }
+}
+
+// All lanes of a warp agree on a bounded wait (tcgen05.ld below is warp-collective).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, ttk::mbar_wait(bar, parity));
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    lmhead_gemm_kernel(const __grid_constant__ LmHeadMaps maps, const LmHeadParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = ttk::smem_u32(smem);
+    const uint32_t bar0 = sbase + kBarOff;
+    auto full_bar = [&](uint32_t st) { return bar0 + 8u * st; };
+    auto empty_bar = [&](uint32_t st) { return bar0 + 8u * (kStages + st); };
+    auto accf_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + a); };
+    auto acce_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
+
+    if (warp == 1) {
+        ttk::tmem_alloc(ttk::smem_u32(tmem_slot), 512);
+        ttk::tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (uint32_t st = 0; st < kStages; ++st) {
+            ttk::mbar_init(full_bar(st), 1);
+            ttk::mbar_init(empty_bar(st), 1);
+        }
+        for (uint32_t a = 0; a < 2; ++a) {
+            ttk::mbar_init(accf_bar(a), 1);
+            ttk::mbar_init(acce_bar(a), 128);
+        }
+        ttk::mbar_init(done_bar, 1);
+        ttk::fence_mbar_init();
+        ttk::prefetch_tensormap(&maps.a);
+        ttk::prefetch_tensormap(&maps.w);
+    }
+    ttk::tc_fence_before();
+    __syncthreads();
+    ttk::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    ttk::pdl_wait();  // the gather kernel's row count, dest[] and a_c
+    ttk::pdl_trigger();
+    const int n_rows = __ldcg(p.n_rows);
+    const Plan pl = make_plan(n_rows, p.V, p.n_ctas);
+    const int items = pl.n_mt * pl.n_chunks;
+    const int nkb = (p.H + 63) / 64;
+    bool ok = true;
+
+    // item -> (row tile, chunk, first and end unit of the chunk)
+    auto item_geom = [&](int item, int& mt, int& chunk, int& u0, int& u1) {
+        mt = item % pl.n_mt;
+        chunk = item / pl.n_mt;
+        u0 = (int)((long long)chunk * pl.units / pl.n_chunks);
+        u1 = (int)((long long)(chunk + 1) * pl.units / pl.n_chunks);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t kc = 0;
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                int mt, chunk, u0, u1;
+                item_geom(item, mt, chunk, u0, u1);
+                for (int ut = u0; ut < u1 && ok; ut += 4) {
+                    const int nbox = min(4, u1 - ut);
+                    for (int kb = 0; kb < nkb; ++kb, ++kc) {
+                        const uint32_t st = kc % kStages;
+                        if (kc >= (uint32_t)kStages && !ttk::mbar_wait(empty_bar(st), ((kc / kStages) - 1) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sA = sbase + st * kStage, sB = sA + kATile;
+                        ttk::mbar_arrive_expect_tx(full_bar(st), kATile + (uint32_t)nbox * kBBox);
+                        ttk::tma_load_2d(sA, &maps.a, kb * 64, mt * 128, full_bar(st));
+                        for (int i = 0; i < nbox; ++i)
+                            ttk::tma_load_2d(sB + (uint32_t)i * kBBox, &maps.w, kb * 64, (ut + i) * 64, full_bar(st));
+                    }
+                }
+            }
+            if (!ok) ttk::report_error(p.um.err, ttk::kErrTimeout);
+            // Drain: the loads of the most recent stages have landed before exit.
+            for (uint32_t j = (kc > (uint32_t)kStages) ? kc - kStages : 0u; j < kc; ++j)
+                ttk::mbar_wait(full_bar(j % kStages), (j / kStages) & 1u);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t kc = 0, it = 0;
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                int mt, chunk, u0, u1;
+                item_geom(item, mt, chunk, u0, u1);
+                for (int ut = u0; ut < u1 && ok; ut += 4, ++it) {
+                    const uint32_t a = it & 1u;
+                    if (it >= 2 && !ttk::mbar_wait(acce_bar(a), ((it >> 1) - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    ttk::tc_fence_after();
+                    for (int kb = 0; kb < nkb; ++kb, ++kc) {
+                        const uint32_t st = kc % kStages;
+                        if (!ttk::mbar_wait(full_bar(st), (kc / kStages) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        ttk::tc_fence_after();
+                        const uint32_t sA = sbase + st * kStage, sB = sA + kATile;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ttk::mma_bf16_ss(tmem + a * 256u, ttk::sdesc_sw128(sA + 32u * k, 16, 1024),
+                                             ttk::sdesc_sw128(sB + 32u * k, 16, 1024), kIdesc,
+                                             (kb > 0 || k > 0) ? 1u : 0u);
+                        ttk::mma_commit(empty_bar(st));  // this stage is no longer read
+                    }
+                    if (ok) ttk::mma_commit(accf_bar(a));
+                }
+            }
+            if (!ok) ttk::report_error(p.um.err, ttk::kErrTimeout);
+            // Everything issued has completed before shared memory and TMEM are released.
+            ttk::mma_commit(done_bar);
+            ttk::mbar_wait(done_bar, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;  // warps 2, 3, 4, 5 -> TMEM lanes 64, 96, 0, 32
+        const int lane_row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float ts = p.um.temp_scale;
+        const int mask = p.um.mask_id;
+        uint32_t it = 0;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            int mt, chunk, u0, u1;
+            item_geom(item, mt, chunk, u0, u1);
+            const int vend = min(p.V, u1 * 64);
+            Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
+            for (int ut = u0; ut < u1; ut += 4, ++it) {
+                const uint32_t a = it & 1u;
+                if (!warp_wait(accf_bar(a), (it >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                ttk::tc_fence_after();
+                const int v = ut * 64;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t r[32];
+                    ttk::tmem_ld32(tmem + lane_off + a * 256u + 32u * c, r);
+                    ttk::tmem_ld_wait32(r);
+                    float x[32];
+                    int id[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int col = v + 32 * c + e;
+                        id[e] = col;
+                        x[e] = (col < vend && col != mask) ? __uint_as_float(r[e]) : -CUDART_INF_F;
+                    }
+                    fold<32>(acc, x, id, ts);
+                }
+                ttk::tc_fence_before();
+                ttk::mbar_arrive(acce_bar(a));
+            }
+            if (!ok) break;
+            const int cr = mt * 128 + lane_row;
+            if (cr < n_rows)
+                __stcg(reinterpret_cast<float4*>(p.part + (size_t)cr * pl.n_chunks + chunk), as_f4(acc));
+        }
+        if (!ok) ttk::report_error(p.um.err, ttk::kErrTimeout);
+    }
+    ttk::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ttk::tc_fence_after();
+        ttk::tmem_dealloc(tmem, 512);
+    }
+}
+
+__global__ void __launch_bounds__(32) lmhead_finish_kernel(LmHeadParams p) {
+    ttk::pdl_wait();  // the GEMM's partials (and, through it, the gather's dest[])
+    ttk::pdl_trigger();
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const UnmaskParams& u = p.um;
+    const Plan pl = make_plan(__ldcg(p.n_rows), p.V, p.n_ctas);
+    if (lane < u.S) {
+        const int row = b * u.S + lane;
+        const int cr = __ldcg(p.dest + row);
+        if (cr >= 0) {
+            const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)cr * pl.n_chunks);
+            Red r{-CUDART_INF_F, 0.f, 0x7fffffff};
+            for (int c = 0; c < pl.n_chunks; ++c) r = combine(r, from_f4(__ldcg(pp + c)), u.temp_scale);
+            __stcg(reinterpret_cast<float4*>(u.row_res) + row, as_f4(r));
+        }
+    }
+    __syncwarp();
+    decide(u, b);
+}
+
+std::mutex g_attr_mu;
+unsigned long long g_attr_done = 0;  // one bit per device ordinal
+
+cudaError_t gemm_prepare() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (dev >= 0 && dev < 64 && ((g_attr_done >> dev) & 1ull)) return cudaSuccess;
+    e = cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) g_attr_done |= (1ull << dev);
+    return e;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+// The compact matrix has whole 128-row tiles, so every TMA box of it is in bounds.
+size_t lmhead_a_rows(int rows) { return ((size_t)rows + 127) / 128 * 128; }
+
+size_t lmhead_workspace_bytes(int B, int S, int H, int n_ctas) {
+    const size_t rows = (size_t)B * S;
+    return align256(lmhead_a_rows((int)rows) * H * 2)        // a_c
+           + align256(rows * 4)                              // dest
+           + 256                                             // n_rows
+           + align256(rows * (size_t)n_ctas * sizeof(UnmaskPartial))  // chunk partials
+           + align256(rows * sizeof(UnmaskPartial))          // row results
+           + align256((rows + B + 1) * sizeof(unsigned int));  // decision tickets
+}
+
+void lmhead_layout(void* ws, LmHeadParams& p) {
+    const size_t rows = (size_t)p.rows;
+    char* w = static_cast<char*>(ws);
+    p.a_c = reinterpret_cast<uint16_t*>(w);
+    w += align256(lmhead_a_rows(p.rows) * p.H * 2);
+    p.dest = reinterpret_cast<int32_t*>(w);
+    w += align256(rows * 4);
+    p.n_rows = reinterpret_cast<int32_t*>(w);
+    w += 256;
+    p.part = reinterpret_cast<UnmaskPartial*>(w);
+    w += align256(rows * (size_t)p.n_ctas * sizeof(UnmaskPartial));
+    p.um.row_res = reinterpret_cast<UnmaskPartial*>(w);
+    w += align256(rows * sizeof(UnmaskPartial));
+    p.um.ticket = reinterpret_cast<unsigned int*>(w);
+    p.um.ticket_words = (int)rows + p.um.B;
+    p.um.part = p.part;
+}
+
+cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStream_t stream) {
+    cudaError_t e = gemm_prepare();
+    if (e != cudaSuccess) return e;
+    const int n_gather = (p.rows + kGatherRows - 1) / kGatherRows;
+    e = launch_pdl(lmhead_gather_kernel, dim3(n_gather), dim3(256), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(lmhead_gemm_kernel, dim3(p.n_ctas), dim3(kGemmThreads), (size_t)kSmemBytes, stream, maps, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(lmhead_finish_kernel, dim3(p.um.B), dim3(32), 0, stream, p);
+}
+
+}  // namespace tti

@@ -498,6 +498,47 @@ tt_status build_block_graph(const tt_step_desc* d, const tt_step_tensors* t, con
     return TT_OK;
 }
 
+tt_status check_sampler(const tt_sampler* sampler) {
+    if (sampler == nullptr) return fail(TT_ERR_INVALID_ARG, "sampler is null");
+    if (sampler->kind < TT_SAMPLER_CONFIDENCE || sampler->kind > TT_SAMPLER_PREDICT_NOISE)
+        return fail(TT_ERR_INVALID_ARG, "sampler kind must be a tt_sampler_kind");
+    if (sampler->max_steps < 1 || sampler->max_steps > 255)
+        return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
+    if (sampler->gamma != sampler->gamma) return fail(TT_ERR_INVALID_ARG, "gamma is NaN");
+    if (!(sampler->temperature > 0.f) || !(sampler->temperature < 1e30f))
+        return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
+    return TT_OK;
+}
+
+// SM count of the current device (one persistent GEMM CTA per SM), cached per device.
+tt_status sm_count(int* out) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    TT_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return TT_OK;
+    }
+    int n = 0;
+    TT_CUDA(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+    if (n < 1) return fail(TT_ERR_CUDA, "device reports no SMs");
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return TT_OK;
+}
+
+// The TMA boxes are 64 wide in H and 64 rows of W, so both extents start at 64.
+tt_status check_lmhead(int B, int S, int H, int V) {
+    if (B < 1 || S < 1) return fail(TT_ERR_INVALID_ARG, "B and S must be >= 1");
+    if (S > 32) return fail(TT_ERR_UNSUPPORTED, "S must be at most 32");
+    if ((long long)B * S > tti::kLmHeadMaxRows) return fail(TT_ERR_UNSUPPORTED, "B*S must be at most 4096");
+    if (H < 64 || H % 8 != 0) return fail(TT_ERR_UNSUPPORTED, "H must be a multiple of 8, at least 64");
+    if (V < 64) return fail(TT_ERR_UNSUPPORTED, "V must be at least 64");
+    return TT_OK;
+}
+
 }  // namespace
 
 // =================================================================================
@@ -868,6 +909,72 @@ tt_status tt_generate(const tt_step_desc* desc, const tt_step_tensors* t, int n_
                                const_cast<int32_t*>(t->ctx_len), t->ids, stop, generated, done,
                                out_tokens, n_blocks * S, k * S, stream));
     }
+    return TT_OK;
+}
+
+size_t tt_lmhead_unmask_workspace(int B, int S, int H) {
+    if (check_lmhead(B, S, H, 64) != TT_OK) return 0;
+    int n = 0;
+    if (sm_count(&n) != TT_OK) return 0;
+    return tti::lmhead_workspace_bytes(B, S, H, n);
+}
+
+tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32_t* ids, int32_t* n_masked,
+                           int32_t* steps, float* conf, uint8_t* commit, uint8_t* commit_step, int B,
+                           int S, int H, int V, int32_t mask_id, const tt_sampler* sampler,
+                           void* workspace, size_t workspace_bytes, tt_stream_t stream) {
+    TT_TRY(check_lmhead(B, S, H, V));
+    TT_TRY(check_sampler(sampler));
+    if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
+    TT_TRY(need_ptr(hidden, "hidden"));
+    TT_TRY(need_ptr(w_vocab, "w_vocab"));
+    TT_TRY(need_ptr(ids, "ids", false));
+    TT_TRY(need_ptr(steps, "steps", false));
+    int n_ctas = 0;
+    TT_TRY(sm_count(&n_ctas));
+    TT_TRY(check_ws(workspace, workspace_bytes, tti::lmhead_workspace_bytes(B, S, H, n_ctas)));
+    int* err = nullptr;
+    TT_TRY(device_err_word(&err));
+    tti::LmHeadParams p{};
+    p.h = static_cast<const uint16_t*>(hidden);
+    p.rows = B * S;
+    p.H = H;
+    p.V = V;
+    p.n_ctas = n_ctas;
+    tti::UnmaskParams& u = p.um;
+    u.logits = nullptr;
+    u.ids = ids;
+    u.n_masked = n_masked;
+    u.steps = steps;
+    u.conf = conf;
+    u.commit = commit;
+    u.commit_step = commit_step;
+    u.B = B;
+    u.S = S;
+    u.V = V;
+    u.mask_id = mask_id;
+    u.gamma = sampler->gamma;
+    u.max_steps = sampler->max_steps;
+    u.mode = sampler->kind;
+    u.temp_scale = temp_scale(sampler->temperature);
+    u.chunk = 0;
+    u.n_chunks = 0;
+    u.err = err;
+    tti::lmhead_layout(workspace, p);
+    tti::LmHeadMaps maps;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)tti::lmhead_a_rows(p.rows)};
+        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t box[2] = {64, 128};
+        TT_TRY(encode_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a_c, dims, strides, box));
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)V};
+        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t box[2] = {64, 64};
+        TT_TRY(encode_map(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_vocab, dims, strides, box));
+    }
+    TT_CUDA(tti::launch_lmhead(p, maps, reinterpret_cast<cudaStream_t>(stream)));
     return TT_OK;
 }
 

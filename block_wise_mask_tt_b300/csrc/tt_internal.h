@@ -99,6 +99,34 @@ constexpr size_t kUnmaskNoallocScratchBytes = size_t(8) << 20;
 // Device address of that array on the current device (looked up once per device).
 cudaError_t unmask_noalloc_scratch(void** out);
 
+// ------------------------------------------------------------- LM head + unmasking
+// The hidden rows of masked positions are gathered into a compact bf16 matrix; a
+// persistent tcgen05 GEMM multiplies it with the vocabulary projection W [V][H] and
+// reduces every (row, vocabulary chunk) to (max, sum of exponentials, lowest argmax)
+// in its epilogue, so no logit is written; a last kernel merges a row's chunks and
+// takes the per-sequence decision of the sampler.
+constexpr int kLmHeadMaxRows = 4096;  // B * S
+struct LmHeadParams {
+    const uint16_t* h;     // [B*S][H] bf16 hidden rows
+    uint16_t* a_c;         // [B*S][H] masked rows, compacted (workspace)
+    int32_t* dest;         // [B*S] compact index of each row, -1 when decoded (workspace)
+    int32_t* n_rows;       // number of masked rows (workspace)
+    UnmaskPartial* part;   // [B*S][max_chunks] per (compact row, vocabulary chunk) (workspace)
+    int rows;              // B * S
+    int H, V;
+    int n_ctas;            // GEMM grid: one persistent CTA per SM
+    UnmaskParams um;       // ids, steps, outputs, sampler, row_res, ticket (decision)
+};
+struct LmHeadMaps {
+    CUtensorMap a;  // a_c: (H, B*S) bf16, box 64 x 128, 128-B swizzle
+    CUtensorMap w;  // W: (H, V) bf16, box 64 x 64, 128-B swizzle
+};
+size_t lmhead_a_rows(int rows);  // rows of a_c: B*S rounded up to a multiple of 128
+size_t lmhead_workspace_bytes(int B, int S, int H, int n_ctas);
+// Fills the workspace pointers of p (p.rows, p.n_ctas set by the caller).
+void lmhead_layout(void* ws, LmHeadParams& p);
+cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStream_t stream);
+
 // -------------------------------------------------------------------------- attention
 struct AttnGeom {
     int B, S, Hq, Hkv, G, D;

@@ -98,6 +98,9 @@ _SIGS = {
                                ctypes.POINTER(tt_sampler), _P, ctypes.c_size_t, _P]),
     "tt_confidence_unmask_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_int32,
                                           ctypes.c_float, _I, _P]),
+    "tt_lmhead_unmask_workspace": (ctypes.c_size_t, [_I, _I, _I]),
+    "tt_lmhead_unmask": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_int32,
+                              ctypes.POINTER(tt_sampler), _P, ctypes.c_size_t, _P]),
     "tt_denoise_workspace": (ctypes.c_size_t, [ctypes.POINTER(tt_step_desc)]),
     "tt_append_block": (_I, [ctypes.POINTER(tt_attn_dims), _P, _P, _P, _P, _P, _P, _P,
                              ctypes.POINTER(tt_stop_spec), _P, _P, _P, _I, _I, _P]),
@@ -235,6 +238,24 @@ def tt_sampler_unmask(logits, ids, steps, B, S, V, mask_id, sampler: tt_sampler,
         _ptr(conf, "conf", _F32, B * S), _ptr(commit, "commit", _U8, B * S),
         _ptr(commit_step, "commit_step", _U8, B * S), B, S, V, int(mask_id),
         ctypes.byref(sampler), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def tt_lmhead_unmask_workspace(B, S, H) -> int:
+    return int(lib.tt_lmhead_unmask_workspace(B, S, H))
+
+
+def tt_lmhead_unmask(hidden, w_vocab, ids, steps, B, S, H, V, mask_id, sampler: tt_sampler,
+                     n_masked=None, conf=None, commit=None, commit_step=None, ws=None,
+                     stream=None) -> None:
+    if ws is None:
+        ws = workspace(tt_lmhead_unmask_workspace(B, S, H), hidden.device)
+    _check(lib.tt_lmhead_unmask(
+        _ptr(hidden, "hidden", _BF16, B * S * H), _ptr(w_vocab, "w_vocab", _BF16, V * H),
+        _ptr(ids, "ids", _I32, B * S), _ptr(n_masked, "n_masked", _I32, B),
+        _ptr(steps, "steps", _I32, B), _ptr(conf, "conf", _F32, B * S),
+        _ptr(commit, "commit", _U8, B * S), _ptr(commit_step, "commit_step", _U8, B * S),
+        B, S, H, V, int(mask_id), ctypes.byref(sampler), ws.data_ptr(), ws.numel(),
+        _stream(stream)))
 
 
 def tt_confidence_unmask_noalloc(logits, ids, steps, B, S, V, mask_id, gamma, max_steps,

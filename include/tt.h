@@ -247,6 +247,39 @@ TT_API tt_status tt_sampler_unmask(const float* logits, int32_t* ids, int32_t* n
                                    size_t workspace_bytes, tt_stream_t stream);
 
 /* --------------------------------------------------------------------------------
+ * tt_lmhead_unmask: one sampler step whose logits come from the LM head, fused so
+ * that the logits are never written to memory.
+ *
+ * "Nemotron-Labs-TwoTower" wiki, "Block-wise generation": every step predicts all
+ * masked positions of the block and commits the confident ones.  For every masked
+ * position (ids[b][s] == mask_id) the logits are
+ *     logit[j] = sum_k hidden[b][s][k] * w_vocab[j][k]      (fp32 accumulation)
+ * and the step is then exactly that of tt_sampler_unmask on those logits (same
+ * confidence, token, tie rules, decision and outputs).  The product runs on the
+ * tensor cores and each (row, vocabulary chunk) is reduced to (max, sum of
+ * exponentials, lowest argmax) as it leaves the accumulator.
+ *
+ *   hidden     bf16 [B][S][H], device, 16-byte aligned: the hidden row of every
+ *              position (rows of decoded positions are not read)
+ *   w_vocab    bf16 [V][H], device, 16-byte aligned: row j projects onto token id j
+ *   ids ... commit_step, mask_id, sampler: as tt_sampler_unmask (sampler is a host
+ *              pointer)
+ *   workspace  tt_lmhead_unmask_workspace(B, S, H) bytes on the current device,
+ *              16-byte aligned; its contents on entry do not matter
+ * Limits: S <= 32, B*S <= 4096, H a multiple of 8 and >= 64, V >= 64.  Invalid
+ * arguments return an error and launch nothing.  Three kernels are launched on
+ * `stream`; a wait inside the GEMM that runs out sets the device error word
+ * (tt_device_status) instead of hanging.
+ * -------------------------------------------------------------------------------- */
+TT_API size_t tt_lmhead_unmask_workspace(int B, int S, int H);
+
+TT_API tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32_t* ids,
+                                  int32_t* n_masked, int32_t* steps, float* conf,
+                                  uint8_t* commit, uint8_t* commit_step, int B, int S, int H,
+                                  int V, int32_t mask_id, const tt_sampler* sampler,
+                                  void* workspace, size_t workspace_bytes, tt_stream_t stream);
+
+/* --------------------------------------------------------------------------------
  * tt_confidence_unmask_noalloc: the same confidence-unmasking step, for callers that
  * cannot provide a workspace.  The pages describing the method have no counterpart
  * to this entry point; it exists for callers whose device memory is owned entirely
