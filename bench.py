@@ -58,11 +58,16 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.5,
                     help="keep warming up for at least this long so the clock sampler sees load")
-    ap.add_argument("--kernel-only", choices=("attn", "unmask", "adaln", "logits", "step"),
+    ap.add_argument("--kernel-only", choices=("attn", "unmask", "adaln", "logits", "step", "lmhead"),
                     default=None,
                     help="profiling aid: run only --reps standalone calls of one entry point on "
                          "the workload (after 3 untimed ones) and print their mean time")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--lm-head", action="store_true",
+                    help="the step's logits come from the fused LM head over the adaLN output "
+                         "(synthetic projection W [V][H]) instead of the hash stand-in")
+    ap.add_argument("--no-lm-head-leg", action="store_true",
+                    help="skip the standalone timing of the fused LM head + sampler step")
     ap.add_argument("--generate", type=int, default=32,
                     help="also time tt_generate over this many blocks (Algorithm 1's outer loop: "
                          "decode, append the block to the cache, next block); 0 skips it")
@@ -197,11 +202,13 @@ class Workbench:
     """Device-resident inputs, state and buffers for one replica of the workload."""
 
     def __init__(self, tt, torch, w: synth.Workload, seed: int, sampler: int = 0,
-                 temperature: float = 1.0):
+                 temperature: float = 1.0, lm_head: bool = False):
         self.tt, self.torch, self.w, self.seed = tt, torch, w, seed
+        self.lm_head = lm_head
         t0 = time.time()
         self.inp = synth.make_attention_inputs(w, seed)
         self.ad = synth.make_adaln_inputs(w, seed)
+        self.w_vocab = self._dev(synth.make_lmhead_weights(w, seed)) if lm_head else None
         self.gen_s = time.time() - t0
         B, S = w.B, w.S
         dev = lambda a: self._dev(a)
@@ -226,11 +233,13 @@ class Workbench:
             commit_step=T.zeros((B, S), dtype=T.uint8, device="cuda"),
             y=T.empty((B, S, w.H), dtype=T.int16, device="cuda"),
             attn_out=T.empty((B, S, w.Hq, w.D), dtype=T.int16, device="cuda"),
-            logits=T.empty((B, S, w.V), dtype=T.float32, device="cuda"),
+            logits=None if lm_head else T.empty((B, S, w.V), dtype=T.float32, device="cuda"),
             conf=T.empty((B, S), dtype=T.float32, device="cuda"),
-            commit=T.empty((B, S), dtype=T.uint8, device="cuda"))
+            commit=T.empty((B, S), dtype=T.uint8, device="cuda"),
+            w_vocab=self.w_vocab)
+        kind = tt.LOGITS_LM_HEAD if lm_head else w.logits_kind
         self.desc = tt.step_desc(self.dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps,
-                                 seed, 0, w.logits_kind, w.boost_lo, w.boost_hi, sampler=sampler,
+                                 seed, 0, kind, w.boost_lo, w.boost_hi, sampler=sampler,
                                  temperature=temperature)
         self.ts = tt.step_tensors(**self.t)
         self.ws = tt.workspace(tt.tt_denoise_workspace(self.desc))
@@ -287,13 +296,14 @@ def run_timed(wb: Workbench, plan, flush, with_events=True):
         wb.reset()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
+        per_step = 6 if wb.lm_head else 5  # adaLN, split, merge, then logits + unmask or the LM head's 3
         if take == n:
             wb.block(bi)
-            launches += 2 + 6 * n  # dyn-slot write + count, then 6 kernels per step
+            launches += 2 + (per_step + 1) * n  # dyn-slot write + count, then the step and loop_cond
         else:
             for _ in range(take):
                 wb.step(bi)
-            launches += 5 * take
+            launches += per_step * take
         e.record()
         e.synchronize()
         elapsed += s.elapsed_time(e) / 1e3
@@ -313,6 +323,8 @@ def kernel_times(wb: Workbench, flush, reps: int):
     steps = torch.zeros(B, dtype=torch.int32, device="cuda")
     spec = tt.tt_logits_spec(wb.seed, 0, w.logits_kind, w.boost_lo, w.boost_hi)
     logits = wb.t["logits"]
+    if logits is None:  # the step runs the LM head; the stand-in unmask is timed on its own buffer
+        logits = torch.empty((B, S, w.V), dtype=torch.float32, device="cuda")
     tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
     res = {}
     for name in ("attn", "unmask"):
@@ -342,6 +354,56 @@ def kernel_times(wb: Workbench, flush, reps: int):
     return res
 
 
+def lmhead_cost(w: synth.Workload, rows: int):
+    """Algorithmic FLOPs and bytes of one fused LM-head call over `rows` masked rows:
+    2 * rows * H * V multiply-adds; W [V][H] and the hidden rows read once (bf16)."""
+    return 2.0 * rows * w.H * w.V, float(w.V * w.H * 2 + rows * w.H * 2)
+
+
+def run_lmhead(wb: Workbench, flush, reps: int = 5):
+    """Standalone tt_lmhead_unmask calls on the workload's shape (every row masked, as
+    at the first step of a block), L2 flushed before each; returns the leg's dict."""
+    tt, torch, w = wb.tt, wb.torch, wb.w
+    B, S = w.B, w.S
+    if B * S > 4096:
+        return None
+    W = wb.w_vocab if wb.w_vocab is not None else wb._dev(synth.make_lmhead_weights(w, wb.seed))
+    h = wb._dev(synth.make_hidden(w, wb.seed))
+    ids = torch.full((B, S), w.mask_id, dtype=torch.int32, device="cuda")
+    steps = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ws = tt.workspace(tt.tt_lmhead_unmask_workspace(B, S, w.H))
+    smp = tt.tt_sampler(int(wb.desc.sampler), w.gamma, float(wb.desc.temperature), w.steps_max)
+    stream = torch.cuda.current_stream()
+    ts = []
+    for r in range(reps + 2):
+        flush()
+        ids.fill_(w.mask_id)
+        steps.zero_()
+        torch.cuda._sleep(200_000)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        tt.tt_lmhead_unmask(h, W, ids, steps, B, S, w.H, w.V, w.mask_id, smp, ws=ws)
+        e.record(stream)
+        e.synchronize()
+        if r >= 2:
+            ts.append(s.elapsed_time(e) / 1e3)
+    if tt.tt_device_status(True) != 0:
+        raise RuntimeError("device-side error reported by tt_lmhead_unmask")
+    t = statistics.mean(ts)
+    flops, byts = lmhead_cost(w, B * S)
+    peaks, kind = load_peaks()
+    tc, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    bound = "tensor" if flops / (tc * 1e12) >= byts / (hbm * 1e9) else "hbm"
+    achieved = flops / t / 1e12 if bound == "tensor" else byts / t / 1e9
+    peak = tc if bound == "tensor" else hbm
+    return {"us": t * 1e6, "rows": B * S, "H": w.H, "V": w.V, "flops": flops, "algorithmic_bytes": byts,
+            "bound": bound, "achieved": achieved, "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+            "peak": peak, "frac": achieved / peak, "peak_source": kind,
+            "TFLOP_s": flops / t / 1e12, "GB_s": byts / t / 1e9,
+            "roofline_us": max(flops / (tc * 1e12), byts / (hbm * 1e9)) * 1e6,
+            "call": "tt_lmhead_unmask, every row masked (first step of a block), L2 flushed"}
+
+
 def kernel_only(wb: Workbench, which: str, reps: int):
     """Standalone calls of one entry point, for profiler captures (no JSON bench line)."""
     tt, torch, w = wb.tt, wb.torch, wb.w
@@ -354,8 +416,15 @@ def kernel_only(wb: Workbench, which: str, reps: int):
     steps = torch.zeros(B, dtype=torch.int32, device="cuda")
     spec = tt.tt_logits_spec(wb.seed, 0, w.logits_kind, w.boost_lo, w.boost_hi)
     logits = wb.t["logits"]
+    if logits is None:  # the step runs the LM head; the stand-in unmask is timed on its own buffer
+        logits = torch.empty((B, S, w.V), dtype=torch.float32, device="cuda")
     tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
     y = torch.empty((B, S, w.H), dtype=torch.int16, device="cuda")
+    if which == "lmhead":
+        W = wb.w_vocab if wb.w_vocab is not None else wb._dev(synth.make_lmhead_weights(w, wb.seed))
+        h = wb._dev(synth.make_hidden(w, wb.seed))
+        lm_ws = tt.workspace(tt.tt_lmhead_unmask_workspace(B, S, w.H))
+        smp = tt.tt_sampler(int(wb.desc.sampler), w.gamma, float(wb.desc.temperature), w.steps_max)
 
     def call():
         if which == "attn":
@@ -371,6 +440,10 @@ def kernel_only(wb: Workbench, which: str, reps: int):
                                  eps=w.ln_eps, row_index=wb.t["n_masked"], table_rows=S + 1)
         elif which == "logits":
             tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
+        elif which == "lmhead":
+            ids.copy_(ids0)
+            steps.zero_()
+            tt.tt_lmhead_unmask(h, W, ids, steps, B, S, w.H, w.V, w.mask_id, smp, ws=lm_ws)
         else:
             wb.reset()
             wb.step(0)
@@ -442,7 +515,7 @@ def run_generate(wb: Workbench, n_blocks: int, flush, reps: int = 3):
     ctx0 = wb.t["ctx_len"].clone()
     dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, cap, 0, 0, 0, w.softmax_scale, 0)
     desc = tt.step_desc(dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps, wb.seed, 0,
-                        w.logits_kind, w.boost_lo, w.boost_hi, sampler=wb.desc.sampler,
+                        wb.desc.logits.kind, w.boost_lo, w.boost_hi, sampler=wb.desc.sampler,
                         temperature=wb.desc.temperature)
     t = dict(wb.t)
     t.update(k_ctx=kc, v_ctx=vc, ctx_len=ctx0.clone())
@@ -606,7 +679,7 @@ def main():
 
     w = workload(args)
     seed = replica_seed(args.seed, rank)
-    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature)
+    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head)
     if args.kernel_only:
         kernel_only(wb, args.kernel_only, args.reps)
         return
@@ -660,8 +733,18 @@ def main():
                                  "roofline_us": wb.unmask_bytes_full / (hbm * 1e9) * 1e6,
                                  "frac": um_gbs / hbm, "algorithmic_bytes": wb.unmask_bytes_full},
     }
-    dominant = "attn" if ktimes["attn"] >= ktimes["unmask"] else "unmask"
-    if dominant == "attn":
+    lm = None if args.no_lm_head_leg and not args.lm_head else run_lmhead(wb, flush)
+    if lm is not None:
+        kernels["tt_lmhead_unmask"] = {k: lm[k] for k in ("us", "TFLOP_s", "GB_s", "bound", "roofline_us",
+                                                           "frac", "algorithmic_bytes", "flops")}
+    if args.lm_head:
+        dominant = "attn" if ktimes["attn"] >= lm["us"] * 1e-6 else "lmhead"
+    else:
+        dominant = "attn" if ktimes["attn"] >= ktimes["unmask"] else "unmask"
+    if dominant == "lmhead":
+        roof = {"kernel": "tt_lmhead_unmask (gather + GEMM + decision, first step)", "bound": lm["bound"],
+                "achieved": lm["achieved"], "peak": lm["peak"], "unit": lm["unit"], "frac": lm["frac"]}
+    elif dominant == "attn":
         if attn_bound == "hbm":
             roof = {"kernel": "tt_denoise_attn (split + merge)", "bound": "hbm", "achieved": attn_gbs,
                     "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm}
@@ -705,6 +788,8 @@ def main():
         "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
                    "D": w.D, "H": w.H, "V": w.V, "gamma": w.gamma, "paged": w.paged,
                    "bench_step": "one denoise step of the whole batch",
+                   "logits": ("fused LM head over the adaLN output (synthetic W [V][H], resident)"
+                              if args.lm_head else "hash stand-in"),
                    "sampler": args.sampler, "temperature": args.temperature,
                    "blocks_timed": len(plan), "whole_blocks": blocks_full,
                    "tokens_per_step": w.B * w.S * blocks_full / max(1, sum(t for _, n, t in plan if t == n)),
@@ -717,6 +802,7 @@ def main():
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "generate": gen_line,
+        "lm_head": lm,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -357,6 +357,8 @@ void lmhead_layout(void* ws, LmHeadParams& p) {
     p.um.part = p.part;
 }
 
+cudaError_t lmhead_prepare() { return gemm_prepare(); }
+
 cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStream_t stream) {
     cudaError_t e = gemm_prepare();
     if (e != cudaSuccess) return e;

@@ -263,6 +263,95 @@ tt_status check_vocab(int B, int S, int V) {
     return TT_OK;
 }
 
+tt_status check_sampler(const tt_sampler* sampler) {
+    if (sampler == nullptr) return fail(TT_ERR_INVALID_ARG, "sampler is null");
+    if (sampler->kind < TT_SAMPLER_CONFIDENCE || sampler->kind > TT_SAMPLER_PREDICT_NOISE)
+        return fail(TT_ERR_INVALID_ARG, "sampler kind must be a tt_sampler_kind");
+    if (sampler->max_steps < 1 || sampler->max_steps > 255)
+        return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
+    if (sampler->gamma != sampler->gamma) return fail(TT_ERR_INVALID_ARG, "gamma is NaN");
+    if (!(sampler->temperature > 0.f) || !(sampler->temperature < 1e30f))
+        return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
+    return TT_OK;
+}
+
+// SM count of the current device (one persistent GEMM CTA per SM), cached per device.
+tt_status sm_count(int* out) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    TT_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return TT_OK;
+    }
+    int n = 0;
+    TT_CUDA(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+    if (n < 1) return fail(TT_ERR_CUDA, "device reports no SMs");
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return TT_OK;
+}
+
+// The TMA boxes are 64 wide in H and 64 rows of W, so both extents start at 64.
+tt_status check_lmhead(int B, int S, int H, int V) {
+    if (B < 1 || S < 1) return fail(TT_ERR_INVALID_ARG, "B and S must be >= 1");
+    if (S > 32) return fail(TT_ERR_UNSUPPORTED, "S must be at most 32");
+    if ((long long)B * S > tti::kLmHeadMaxRows) return fail(TT_ERR_UNSUPPORTED, "B*S must be at most 4096");
+    if (H < 64 || H % 8 != 0) return fail(TT_ERR_UNSUPPORTED, "H must be a multiple of 8, at least 64");
+    if (V < 64) return fail(TT_ERR_UNSUPPORTED, "V must be at least 64");
+    return TT_OK;
+}
+
+// The three kernels of the fused LM head + sampler step (arguments already checked).
+tt_status enqueue_lmhead(const void* hidden, const void* w_vocab, int32_t* ids, int32_t* n_masked,
+                         int32_t* steps, float* conf, uint8_t* commit, uint8_t* commit_step, int B,
+                         int S, int H, int V, int32_t mask_id, int kind, float gamma, int max_steps,
+                         float temperature, int n_ctas, void* ws, int* err, cudaStream_t st) {
+    tti::LmHeadParams p{};
+    p.h = static_cast<const uint16_t*>(hidden);
+    p.rows = B * S;
+    p.H = H;
+    p.V = V;
+    p.n_ctas = n_ctas;
+    tti::UnmaskParams& u = p.um;
+    u.logits = nullptr;
+    u.ids = ids;
+    u.n_masked = n_masked;
+    u.steps = steps;
+    u.conf = conf;
+    u.commit = commit;
+    u.commit_step = commit_step;
+    u.B = B;
+    u.S = S;
+    u.V = V;
+    u.mask_id = mask_id;
+    u.gamma = gamma;
+    u.max_steps = max_steps;
+    u.mode = kind;
+    u.temp_scale = temp_scale(temperature);
+    u.chunk = 0;
+    u.n_chunks = 0;
+    u.err = err;
+    tti::lmhead_layout(ws, p);
+    tti::LmHeadMaps maps;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)tti::lmhead_a_rows(p.rows)};
+        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t box[2] = {64, 128};
+        TT_TRY(encode_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a_c, dims, strides, box));
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)V};
+        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t box[2] = {64, 64};
+        TT_TRY(encode_map(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_vocab, dims, strides, box));
+    }
+    TT_CUDA(tti::launch_lmhead(p, maps, st));
+    return TT_OK;
+}
+
 // ------------------------------------------------------------- step (shared pieces)
 struct StepPlan {
     AttnPlan attn;
@@ -270,6 +359,8 @@ struct StepPlan {
     size_t unmask_ws_off;
     size_t dyn_off;   // {seed, block_index, loop iteration} for the block graph
     size_t total;
+    bool lm_head;     // logits from the fused LM head (else the stand-in + unmask)
+    int n_ctas;       // LM-head GEMM grid
 };
 
 tt_status plan_step(const tt_step_desc* d, StepPlan& sp) {
@@ -281,15 +372,25 @@ tt_status plan_step(const tt_step_desc* d, StepPlan& sp) {
     if (d->max_steps < 1 || d->max_steps > 255) return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
     if (d->mask_id < 0 || d->mask_id >= d->V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
     if (!(d->ln_eps >= 0.f)) return fail(TT_ERR_INVALID_ARG, "ln_eps must be >= 0");
-    if (d->logits.kind != 0 && d->logits.kind != 1) return fail(TT_ERR_INVALID_ARG, "logits.kind must be 0 or 1");
+    if (d->logits.kind < 0 || d->logits.kind > TT_LOGITS_LM_HEAD)
+        return fail(TT_ERR_INVALID_ARG, "logits.kind must be 0, 1 or TT_LOGITS_LM_HEAD");
     if (d->sampler < TT_SAMPLER_CONFIDENCE || d->sampler > TT_SAMPLER_PREDICT_NOISE)
         return fail(TT_ERR_INVALID_ARG, "sampler must be a tt_sampler_kind");
     if (!(d->temperature > 0.f) || !(d->temperature < 1e30f))
         return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
+    sp.lm_head = d->logits.kind == TT_LOGITS_LM_HEAD;
+    sp.n_ctas = 0;
+    size_t tail_ws = 0;
+    if (sp.lm_head) {
+        TT_TRY(check_lmhead(d->attn.B, d->attn.S, d->H, d->V));
+        TT_TRY(sm_count(&sp.n_ctas));
+        tail_ws = tti::lmhead_workspace_bytes(d->attn.B, d->attn.S, d->H, sp.n_ctas);
+    } else {
+        tail_ws = tti::unmask_workspace_bytes(d->attn.B, d->attn.S, d->V);
+    }
     sp.attn_ws = (tti::attn_workspace_bytes(sp.attn.g) + 255) & ~size_t(255);
     sp.unmask_ws_off = sp.attn_ws;
-    sp.dyn_off = (sp.attn_ws + tti::unmask_workspace_bytes(d->attn.B, d->attn.S, d->V) + 255) &
-                 ~size_t(255);
+    sp.dyn_off = (sp.attn_ws + tail_ws + 255) & ~size_t(255);
     sp.total = sp.dyn_off + 256;
     return TT_OK;
 }
@@ -304,9 +405,13 @@ tt_status check_step_tensors(const tt_step_desc* d, const tt_step_tensors* t) {
     TT_TRY(need_ptr(t->steps, "steps", false));
     TT_TRY(need_ptr(t->commit_step, "commit_step", false));
     TT_TRY(need_ptr(t->y, "y"));
-    TT_TRY(need_ptr(t->logits, "logits"));
+    if (d->logits.kind == TT_LOGITS_LM_HEAD) {
+        TT_TRY(need_ptr(t->w_vocab, "w_vocab"));
+        TT_CUDA(tti::lmhead_prepare());
+    } else {
+        TT_TRY(need_ptr(t->logits, "logits"));
+    }
     if (t->y == t->x) return fail(TT_ERR_INVALID_ARG, "y may not alias x");
-    (void)d;
     return TT_OK;
 }
 
@@ -333,41 +438,48 @@ tt_status enqueue_step(const tt_step_desc* d, const tt_step_tensors* t, const St
     TT_TRY(launch_attention(sp.attn, t->q, t->k_blk, t->v_blk, t->page_table, t->ctx_len,
                             t->n_masked, t->attn_out, nullptr, ws, err, st));
 
-    tti::LogitsParams lp;
-    lp.ids = t->ids;
-    lp.steps = t->steps;
-    lp.logits = t->logits;
-    lp.B = B;
-    lp.S = S;
-    lp.V = d->V;
-    lp.mask_id = d->mask_id;
-    lp.seed = d->logits.seed;
-    lp.block_index = d->logits.block_index;
-    lp.kind = d->logits.kind;
-    lp.boost_lo = d->logits.boost_lo;
-    lp.boost_hi = d->logits.boost_hi;
-    lp.dyn = cond ? reinterpret_cast<const uint32_t*>(static_cast<char*>(ws) + sp.dyn_off) : nullptr;
-    TT_CUDA(tti::launch_logits(lp, st));
+    if (sp.lm_head) {
+        TT_TRY(enqueue_lmhead(t->y, t->w_vocab, t->ids, t->n_masked, t->steps, t->conf, t->commit,
+                              t->commit_step, B, S, d->H, d->V, d->mask_id, d->sampler, d->gamma,
+                              d->max_steps, d->temperature, sp.n_ctas,
+                              static_cast<char*>(ws) + sp.unmask_ws_off, err, st));
+    } else {
+        tti::LogitsParams lp;
+        lp.ids = t->ids;
+        lp.steps = t->steps;
+        lp.logits = t->logits;
+        lp.B = B;
+        lp.S = S;
+        lp.V = d->V;
+        lp.mask_id = d->mask_id;
+        lp.seed = d->logits.seed;
+        lp.block_index = d->logits.block_index;
+        lp.kind = d->logits.kind;
+        lp.boost_lo = d->logits.boost_lo;
+        lp.boost_hi = d->logits.boost_hi;
+        lp.dyn = cond ? reinterpret_cast<const uint32_t*>(static_cast<char*>(ws) + sp.dyn_off) : nullptr;
+        TT_CUDA(tti::launch_logits(lp, st));
 
-    tti::UnmaskParams up;
-    up.logits = t->logits;
-    up.ids = t->ids;
-    up.n_masked = t->n_masked;
-    up.steps = t->steps;
-    up.conf = t->conf;
-    up.commit = t->commit;
-    up.commit_step = t->commit_step;
-    up.B = B;
-    up.S = S;
-    up.V = d->V;
-    up.mask_id = d->mask_id;
-    up.gamma = d->gamma;
-    up.max_steps = d->max_steps;
-    up.mode = d->sampler;
-    up.temp_scale = temp_scale(d->temperature);
-    tti::unmask_layout(B, S, d->V, static_cast<char*>(ws) + sp.unmask_ws_off, up);
-    up.err = err;
-    TT_CUDA(tti::launch_unmask(up, st));
+        tti::UnmaskParams up;
+        up.logits = t->logits;
+        up.ids = t->ids;
+        up.n_masked = t->n_masked;
+        up.steps = t->steps;
+        up.conf = t->conf;
+        up.commit = t->commit;
+        up.commit_step = t->commit_step;
+        up.B = B;
+        up.S = S;
+        up.V = d->V;
+        up.mask_id = d->mask_id;
+        up.gamma = d->gamma;
+        up.max_steps = d->max_steps;
+        up.mode = d->sampler;
+        up.temp_scale = temp_scale(d->temperature);
+        tti::unmask_layout(B, S, d->V, static_cast<char*>(ws) + sp.unmask_ws_off, up);
+        up.err = err;
+        TT_CUDA(tti::launch_unmask(up, st));
+    }
     if (cond) {
         tti::LoopCondParams lc;
         lc.n_masked = t->n_masked;
@@ -498,46 +610,6 @@ tt_status build_block_graph(const tt_step_desc* d, const tt_step_tensors* t, con
     return TT_OK;
 }
 
-tt_status check_sampler(const tt_sampler* sampler) {
-    if (sampler == nullptr) return fail(TT_ERR_INVALID_ARG, "sampler is null");
-    if (sampler->kind < TT_SAMPLER_CONFIDENCE || sampler->kind > TT_SAMPLER_PREDICT_NOISE)
-        return fail(TT_ERR_INVALID_ARG, "sampler kind must be a tt_sampler_kind");
-    if (sampler->max_steps < 1 || sampler->max_steps > 255)
-        return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
-    if (sampler->gamma != sampler->gamma) return fail(TT_ERR_INVALID_ARG, "gamma is NaN");
-    if (!(sampler->temperature > 0.f) || !(sampler->temperature < 1e30f))
-        return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
-    return TT_OK;
-}
-
-// SM count of the current device (one persistent GEMM CTA per SM), cached per device.
-tt_status sm_count(int* out) {
-    static std::mutex mu;
-    static int cache[64] = {0};
-    int dev = 0;
-    TT_CUDA(cudaGetDevice(&dev));
-    std::lock_guard<std::mutex> lk(mu);
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
-        *out = cache[dev];
-        return TT_OK;
-    }
-    int n = 0;
-    TT_CUDA(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
-    if (n < 1) return fail(TT_ERR_CUDA, "device reports no SMs");
-    if (dev >= 0 && dev < 64) cache[dev] = n;
-    *out = n;
-    return TT_OK;
-}
-
-// The TMA boxes are 64 wide in H and 64 rows of W, so both extents start at 64.
-tt_status check_lmhead(int B, int S, int H, int V) {
-    if (B < 1 || S < 1) return fail(TT_ERR_INVALID_ARG, "B and S must be >= 1");
-    if (S > 32) return fail(TT_ERR_UNSUPPORTED, "S must be at most 32");
-    if ((long long)B * S > tti::kLmHeadMaxRows) return fail(TT_ERR_UNSUPPORTED, "B*S must be at most 4096");
-    if (H < 64 || H % 8 != 0) return fail(TT_ERR_UNSUPPORTED, "H must be a multiple of 8, at least 64");
-    if (V < 64) return fail(TT_ERR_UNSUPPORTED, "V must be at least 64");
-    return TT_OK;
-}
 
 }  // namespace
 
@@ -935,47 +1007,9 @@ tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32_t* ids
     TT_TRY(check_ws(workspace, workspace_bytes, tti::lmhead_workspace_bytes(B, S, H, n_ctas)));
     int* err = nullptr;
     TT_TRY(device_err_word(&err));
-    tti::LmHeadParams p{};
-    p.h = static_cast<const uint16_t*>(hidden);
-    p.rows = B * S;
-    p.H = H;
-    p.V = V;
-    p.n_ctas = n_ctas;
-    tti::UnmaskParams& u = p.um;
-    u.logits = nullptr;
-    u.ids = ids;
-    u.n_masked = n_masked;
-    u.steps = steps;
-    u.conf = conf;
-    u.commit = commit;
-    u.commit_step = commit_step;
-    u.B = B;
-    u.S = S;
-    u.V = V;
-    u.mask_id = mask_id;
-    u.gamma = sampler->gamma;
-    u.max_steps = sampler->max_steps;
-    u.mode = sampler->kind;
-    u.temp_scale = temp_scale(sampler->temperature);
-    u.chunk = 0;
-    u.n_chunks = 0;
-    u.err = err;
-    tti::lmhead_layout(workspace, p);
-    tti::LmHeadMaps maps;
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)tti::lmhead_a_rows(p.rows)};
-        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-        const cuuint32_t box[2] = {64, 128};
-        TT_TRY(encode_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a_c, dims, strides, box));
-    }
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)V};
-        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-        const cuuint32_t box[2] = {64, 64};
-        TT_TRY(encode_map(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_vocab, dims, strides, box));
-    }
-    TT_CUDA(tti::launch_lmhead(p, maps, reinterpret_cast<cudaStream_t>(stream)));
-    return TT_OK;
+    return enqueue_lmhead(hidden, w_vocab, ids, n_masked, steps, conf, commit, commit_step, B, S, H, V,
+                          mask_id, sampler->kind, sampler->gamma, sampler->max_steps, sampler->temperature,
+                          n_ctas, workspace, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

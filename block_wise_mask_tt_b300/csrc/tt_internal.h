@@ -126,6 +126,7 @@ size_t lmhead_workspace_bytes(int B, int S, int H, int n_ctas);
 // Fills the workspace pointers of p (p.rows, p.n_ctas set by the caller).
 void lmhead_layout(void* ws, LmHeadParams& p);
 cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStream_t stream);
+cudaError_t lmhead_prepare();  // sets the GEMM's shared-memory limit on this device
 
 // -------------------------------------------------------------------------- attention
 struct AttnGeom {

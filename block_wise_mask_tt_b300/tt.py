@@ -58,6 +58,7 @@ class tt_step_desc(ctypes.Structure):
 
 
 SAMPLER_CONFIDENCE, SAMPLER_MOCK_AR, SAMPLER_PREDICT_NOISE = 0, 1, 2
+LOGITS_LM_HEAD = 2  # tt_logits_spec.kind of a step whose logits come from the LM head
 
 
 class tt_stop_spec(ctypes.Structure):
@@ -71,7 +72,7 @@ class tt_sampler(ctypes.Structure):
 
 _STEP_TENSOR_FIELDS = ("x", "shift_table", "scale_table", "q", "k_blk", "v_blk", "k_ctx", "v_ctx",
                        "page_table", "ctx_len", "ids", "n_masked", "steps", "commit_step", "y",
-                       "attn_out", "logits", "conf", "commit")
+                       "attn_out", "logits", "conf", "commit", "w_vocab")
 
 
 class tt_step_tensors(ctypes.Structure):

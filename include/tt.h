@@ -61,7 +61,7 @@ typedef enum {
 } tt_status;
 
 /* ABI revision of this header. */
-#define TT_ABI_VERSION 2
+#define TT_ABI_VERSION 3
 TT_API int tt_abi_version(void);
 
 /* Static name of a status code. */
@@ -165,9 +165,13 @@ TT_API tt_status tt_denoise_attn(const tt_attn_dims* dims, const void* q, const 
 typedef struct {
     uint32_t seed;
     int block_index;
-    int kind;           /* 0 uniform boost, 1 bimodal boost */
+    int kind;           /* 0 uniform boost, 1 bimodal boost; in a step, 2 = the LM head */
     float boost_lo, boost_hi;
 } tt_logits_spec;
+
+/* logits.kind of a step whose logits come from the LM head (tt_lmhead_unmask) over the
+ * step's adaLN output y, with the projection t->w_vocab, instead of the stand-in. */
+#define TT_LOGITS_LM_HEAD 2
 
 TT_API tt_status tt_synthetic_logits(const tt_logits_spec* spec, const int32_t* ids,
                               const int32_t* steps, float* logits, int B, int S, int V,
@@ -320,6 +324,9 @@ TT_API tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids,
  * One step, for every sequence that still has masked positions:
  *   adaLN(x, table row n_masked[b]) -> y; attention -> attn_out; synthetic logits
  *   for the masked rows (step index steps[b]) -> logits; confidence unmasking.
+ * With logits.kind == TT_LOGITS_LM_HEAD the last two are replaced by the fused LM
+ * head and sampler step of tt_lmhead_unmask with hidden = y and W = t->w_vocab (no
+ * logits buffer is used; H >= 64, V >= 64, B*S <= 4096).
  * The adaLN output does not feed the attention queries here: the projections that
  * would connect them need trained weights.
  * -------------------------------------------------------------------------------- */
@@ -356,9 +363,11 @@ typedef struct {
     /* outputs / buffers */
     void* y;                    /* bf16 [B][S][H]: adaLN of the last step   */
     void* attn_out;             /* bf16 [B][S][Hq][D]                       */
-    float* logits;              /* fp32 [B][S][V] buffer                    */
+    float* logits;              /* fp32 [B][S][V] buffer (NULL with the LM head) */
     float* conf;                /* fp32 [B][S] or NULL                      */
     uint8_t* commit;            /* uint8 [B][S] or NULL                     */
+    /* LM head (logits.kind == TT_LOGITS_LM_HEAD), else NULL */
+    const void* w_vocab;        /* bf16 [V][H]                              */
 } tt_step_tensors;
 
 /* Workspace for tt_denoise_step / tt_denoise_block_loop (attention partials, unmask

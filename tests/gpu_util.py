@@ -12,7 +12,14 @@ Comparison rules (tolerances of the parity contract):
 * unmask: token ids, commit masks, step counts bit-exact, except sequences in which a
   masked position's oracle confidence lies within 1e-5 of gamma, or in which the floor
   decides between confidences within 1e-5 (relative) of each other - those are counted
-  and checked for validity only; confidences within 1e-5 relative.
+  and checked for validity only; confidences within 1e-5 relative;
+* fused LM head + sampler step: the kernel accumulates the logits in fp32, so each
+  logit may differ from the exact value by delta = (H/16 + 16) 2^-24 sum_k |h_k W_jk|
+  (H/16 accumulator additions of 16-product slices); tokens equal the oracle's where
+  its top two logits are more than 2 delta apart and lie within 2 delta of the top
+  otherwise; confidences agree within exp(2 delta / tau) - 1 + 1e-5 relative; the
+  decision is bit-exact except in sequences that compare values closer than that
+  (counted, validity only).
 """
 from __future__ import annotations
 
@@ -151,3 +158,86 @@ def run_unmask(tt, logits: np.ndarray, ids0, steps0, cs0, mask_id, gamma, T):
     torch.cuda.synchronize()
     return dict(ids=host(ids), steps=host(steps), n_masked=host(n_masked), conf=host(conf),
                 commit=host(commit), commit_step=host(cs))
+
+
+def _abs_bound(hr, W, rows=16384):
+    """max_j sum_k |h_rk W_jk| for every row of hr (bf16 bits), W in blocks of rows."""
+    ha = np.abs(oracle.lmhead.bf16_bits_to_f64(hr))
+    out = np.zeros(hr.shape[0])
+    for v0 in range(0, W.shape[0], rows):
+        Wa = np.abs(oracle.lmhead.bf16_bits_to_f64(W[v0:v0 + rows]))
+        out = np.maximum(out, (ha @ Wa.T).max(axis=1))
+    return out
+
+
+def compare_lmhead(gpu, h, W, ids0, steps0, cs0, mask, kind, gamma, T, tau, seqs=None):
+    """Parity of one fused LM-head sampler step (see the lmhead rules in the module
+    docstring); returns the number of sequences checked for validity only."""
+    B, S, H = h.shape
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    rows = [(b, p) for b in seqs for p in np.flatnonzero(ids0[b] == mask)]
+    if rows:
+        hr = np.stack([h[b][p] for b, p in rows])
+        lg_all = oracle.lm_head_logits(hr, W)  # the oracle's exact logits of every sampled row
+        bound_all = _abs_bound(hr, W)
+    excluded = 0
+    at = 0
+    for b in seqs:
+        masked = ids0[b] == mask
+        pos = np.flatnonzero(masked)
+        lg = lg_all[at:at + pos.size].copy() if pos.size else None
+        delta = (H / 16 + 16) * 2.0 ** -24 * bound_all[at:at + pos.size] if pos.size else None
+        at += pos.size
+
+        def rows_of(positions, lg=lg, pos=pos):
+            assert list(positions) == pos.tolist()
+            return lg
+        r = oracle.sampler_step(rows_of, ids0[b], int(steps0[b]), mask, T, kind, gamma, tau, cs0[b])
+        assert np.all(gpu["conf"][b][~masked] == 0.0), f"b={b}: conf of a decoded position"
+        if not masked.any():
+            assert np.array_equal(gpu["ids"][b], ids0[b]) and gpu["steps"][b] == steps0[b]
+            assert gpu["n_masked"][b] == 0 and not gpu["commit"][b].any()
+            continue
+        lg[:, mask] = -np.inf
+        srt = np.sort(lg, axis=1)
+        gap = srt[:, -1] - srt[:, -2]
+        near_tie = gap <= 2 * delta
+        tol = np.expm1(2 * delta / tau) + 1e-5
+        cg, co = gpu["conf"][b][pos], r["conf"][pos]
+        rel = np.abs(cg - co) / co
+        assert np.all(rel <= tol), f"b={b}: conf rel err {rel.max()} > {tol[np.argmax(rel - tol)]}"
+        ambiguous = bool(near_tie.any())
+        if kind == 0 and np.any(np.abs(co - gamma) <= tol * co):
+            ambiguous = True
+        if kind in (0, 2):
+            k = r["k_min"]
+            n_above = int(np.sum(co >= gamma)) if kind == 0 else 0
+            if n_above < k < pos.size:
+                c_sorted = np.sort(co)[::-1]
+                if c_sorted[k - 1] - c_sorted[k] <= 2 * tol.max() * c_sorted[k - 1]:
+                    ambiguous = True
+        com = gpu["commit"][b].astype(bool)
+        # validity (every sequence): commits only at masked positions, decoded ones kept,
+        # each committed token within 2 delta of the top logit, the rest still masked
+        assert np.all(~com | masked)
+        assert np.array_equal(gpu["ids"][b][~masked], ids0[b][~masked])
+        assert np.all(gpu["ids"][b][masked & ~com] == mask)
+        for j, p_ in enumerate(pos):
+            if com[p_]:
+                t = gpu["ids"][b][p_]
+                assert t != mask and lg[j, t] >= srt[j, -1] - 2 * delta[j], f"b={b} pos={p_}: token {t}"
+        assert gpu["steps"][b] == r["steps"]
+        if kind == 1:
+            assert com.sum() == 1
+        elif kind == 2:
+            assert com.sum() == r["k_min"]
+        else:
+            assert com.sum() >= r["k_min"]
+        if ambiguous:
+            excluded += 1
+            continue
+        assert np.array_equal(gpu["ids"][b], r["ids"]), f"b={b}: ids differ"
+        assert np.array_equal(gpu["commit"][b], r["commit"]), f"b={b}: commit differs"
+        assert gpu["n_masked"][b] == r["n_masked"], f"b={b}: n_masked"
+        assert np.array_equal(gpu["commit_step"][b], r["commit_step"]), f"b={b}: commit_step"
+    return excluded

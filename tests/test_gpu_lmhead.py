@@ -19,7 +19,7 @@ import torch
 
 import oracle
 from block_wise_mask_tt_b300 import synth
-from gpu_util import dev, host
+from gpu_util import compare_lmhead as compare, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -66,88 +66,6 @@ def run_gpu(tt, h, W, ids0, steps0, cs0, mask, kind, gamma, T, tau):
     assert tt.tt_device_status(True) == 0
     return dict(ids=host(ids), steps=host(steps), n_masked=host(n_masked), conf=host(conf),
                 commit=host(commit), commit_step=host(cs))
-
-
-def _abs_bound(hr, W, rows=16384):
-    """max_j sum_k |h_rk W_jk| for every row of hr (bf16 bits), W in blocks of rows."""
-    ha = np.abs(oracle.lmhead.bf16_bits_to_f64(hr))
-    out = np.zeros(hr.shape[0])
-    for v0 in range(0, W.shape[0], rows):
-        Wa = np.abs(oracle.lmhead.bf16_bits_to_f64(W[v0:v0 + rows]))
-        out = np.maximum(out, (ha @ Wa.T).max(axis=1))
-    return out
-
-
-def compare(gpu, h, W, ids0, steps0, cs0, mask, kind, gamma, T, tau, seqs=None):
-    """Asserts the rules of the module docstring; returns the number of excluded sequences."""
-    B, S, H = h.shape
-    seqs = list(range(B)) if seqs is None else list(seqs)
-    rows = [(b, p) for b in seqs for p in np.flatnonzero(ids0[b] == mask)]
-    if rows:
-        hr = np.stack([h[b][p] for b, p in rows])
-        lg_all = oracle.lm_head_logits(hr, W)  # the oracle's exact logits of every sampled row
-        bound_all = _abs_bound(hr, W)
-    excluded = 0
-    at = 0
-    for b in seqs:
-        masked = ids0[b] == mask
-        pos = np.flatnonzero(masked)
-        lg = lg_all[at:at + pos.size].copy() if pos.size else None
-        delta = (H / 16 + 16) * 2.0 ** -24 * bound_all[at:at + pos.size] if pos.size else None
-        at += pos.size
-
-        def rows_of(positions, lg=lg, pos=pos):
-            assert list(positions) == pos.tolist()
-            return lg
-        r = oracle.sampler_step(rows_of, ids0[b], int(steps0[b]), mask, T, kind, gamma, tau, cs0[b])
-        assert np.all(gpu["conf"][b][~masked] == 0.0), f"b={b}: conf of a decoded position"
-        if not masked.any():
-            assert np.array_equal(gpu["ids"][b], ids0[b]) and gpu["steps"][b] == steps0[b]
-            assert gpu["n_masked"][b] == 0 and not gpu["commit"][b].any()
-            continue
-        lg[:, mask] = -np.inf
-        srt = np.sort(lg, axis=1)
-        gap = srt[:, -1] - srt[:, -2]
-        near_tie = gap <= 2 * delta
-        tol = np.expm1(2 * delta / tau) + 1e-5
-        cg, co = gpu["conf"][b][pos], r["conf"][pos]
-        rel = np.abs(cg - co) / co
-        assert np.all(rel <= tol), f"b={b}: conf rel err {rel.max()} > {tol[np.argmax(rel - tol)]}"
-        ambiguous = bool(near_tie.any())
-        if kind == CONFIDENCE and np.any(np.abs(co - gamma) <= tol * co):
-            ambiguous = True
-        if kind in (CONFIDENCE, PREDICT_NOISE):
-            k = r["k_min"]
-            n_above = int(np.sum(co >= gamma)) if kind == CONFIDENCE else 0
-            if n_above < k < pos.size:
-                c_sorted = np.sort(co)[::-1]
-                if c_sorted[k - 1] - c_sorted[k] <= 2 * tol.max() * c_sorted[k - 1]:
-                    ambiguous = True
-        com = gpu["commit"][b].astype(bool)
-        # validity (every sequence): commits only at masked positions, decoded ones kept,
-        # each committed token within 2 delta of the top logit, the rest still masked
-        assert np.all(~com | masked)
-        assert np.array_equal(gpu["ids"][b][~masked], ids0[b][~masked])
-        assert np.all(gpu["ids"][b][masked & ~com] == mask)
-        for j, p_ in enumerate(pos):
-            if com[p_]:
-                t = gpu["ids"][b][p_]
-                assert t != mask and lg[j, t] >= srt[j, -1] - 2 * delta[j], f"b={b} pos={p_}: token {t}"
-        assert gpu["steps"][b] == r["steps"]
-        if kind == MOCK_AR:
-            assert com.sum() == 1
-        elif kind == PREDICT_NOISE:
-            assert com.sum() == r["k_min"]
-        else:
-            assert com.sum() >= r["k_min"]
-        if ambiguous:
-            excluded += 1
-            continue
-        assert np.array_equal(gpu["ids"][b], r["ids"]), f"b={b}: ids differ"
-        assert np.array_equal(gpu["commit"][b], r["commit"]), f"b={b}: commit differs"
-        assert gpu["n_masked"][b] == r["n_masked"], f"b={b}: n_masked"
-        assert np.array_equal(gpu["commit_step"][b], r["commit_step"]), f"b={b}: commit_step"
-    return excluded
 
 
 CASES = [

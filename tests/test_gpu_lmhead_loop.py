@@ -1,0 +1,100 @@
+"""The denoise step and block loop with the fused LM head in place of the logits
+stand-in (logits.kind = TT_LOGITS_LM_HEAD): the LM head reads the step's adaLN output.
+
+Each tt_denoise_step is compared with the oracle from the GPU's own pre-step state
+and its own bf16 adaLN output (teacher forcing): the adaLN output against
+oracle.adaln_modulate, the fused LM-head step against oracle.lm_head_logits +
+oracle.sampler_step with the tolerances of gpu_util.compare_lmhead.  Then
+tt_denoise_block_loop must reproduce the step-by-step final state bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_wise_mask_tt_b300 import synth
+from gpu_util import adaln_tol, bf16_to_f64, compare_lmhead, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tt():
+    from block_wise_mask_tt_b300 import tt as _tt
+    return _tt
+
+
+CASES = {
+    "tiny_B3_V4096": synth.CONFIGS[0].replace(B=3, V=4096),
+    "single_B2_L512_V16384": synth.CONFIGS[1].replace(B=2, L=512, V=16384),
+    "paged_B4_S32_V8192": synth.CONFIGS[4].replace(B=4, L=700, L_min=64, V=8192, H=512),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_step_and_loop_with_lm_head(tt, name):
+    w = CASES[name]
+    seed = 5
+    B, S = w.B, w.S
+    inp = synth.make_attention_inputs(w, seed)
+    ad = synth.make_adaln_inputs(w, seed)
+    W = synth.make_lmhead_weights(w, seed)
+    if w.paged:
+        kp = inp["k_pages"]
+        dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, 0, w.page_size, inp["page_table"].shape[1], kp.shape[0],
+                            w.softmax_scale, 0)
+        k_ctx, v_ctx, pt = dev(kp), dev(inp["v_pages"]), dev(inp["page_table"])
+    else:
+        dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, inp["k_ctx"].shape[1], 0, 0, 0, w.softmax_scale, 0)
+        k_ctx, v_ctx, pt = dev(inp["k_ctx"]), dev(inp["v_ctx"]), None
+    desc = tt.step_desc(dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps, seed, 0,
+                        tt.LOGITS_LM_HEAD, 0.0, 0.0)
+    t = dict(x=dev(ad["x"]), shift_table=dev(ad["shift_table"]), scale_table=dev(ad["scale_table"]),
+             q=dev(inp["q"]), k_blk=dev(inp["k_blk"]), v_blk=dev(inp["v_blk"]), k_ctx=k_ctx, v_ctx=v_ctx,
+             page_table=pt, ctx_len=dev(inp["ctx_len"]),
+             ids=torch.full((B, S), w.mask_id, dtype=torch.int32, device="cuda"),
+             n_masked=torch.full((B,), S, dtype=torch.int32, device="cuda"),
+             steps=torch.zeros(B, dtype=torch.int32, device="cuda"),
+             commit_step=torch.zeros((B, S), dtype=torch.uint8, device="cuda"),
+             y=torch.zeros((B, S, w.H), dtype=torch.int16, device="cuda"),
+             attn_out=torch.zeros((B, S, w.Hq, w.D), dtype=torch.int16, device="cuda"),
+             conf=torch.zeros((B, S), dtype=torch.float32, device="cuda"),
+             commit=torch.zeros((B, S), dtype=torch.uint8, device="cuda"),
+             w_vocab=dev(W))
+    ts = tt.step_tensors(**t)
+    ws = tt.workspace(tt.tt_denoise_workspace(desc))
+    excluded = compared = 0
+    for k in range(w.steps_max + 1):
+        ids0, steps0, cs0 = host(t["ids"]), host(t["steps"]), host(t["commit_step"])
+        if not np.any(ids0 == w.mask_id):
+            break
+        n0 = host(t["n_masked"])
+        tt.tt_denoise_step(desc, ts, ws)
+        torch.cuda.synchronize()
+        assert tt.tt_device_status(True) == 0
+        y = host(t["y"])
+        for b in range(B):
+            if n0[b] == 0:
+                continue
+            ref = oracle.adaln_modulate(ad["x"][b], ad["shift_table"][n0[b]].astype(np.float64),
+                                        ad["scale_table"][n0[b]].astype(np.float64), w.ln_eps)
+            err = np.abs(bf16_to_f64(y[b]) - ref)
+            assert np.all(err <= adaln_tol(ref, ad["shift_table"][n0[b]].astype(np.float64))), f"step {k} b={b}"
+        gpu = dict(ids=host(t["ids"]), steps=host(t["steps"]), n_masked=host(t["n_masked"]),
+                   conf=host(t["conf"]), commit=host(t["commit"]), commit_step=host(t["commit_step"]))
+        excluded += compare_lmhead(gpu, y, W, ids0, steps0, cs0, w.mask_id, 0, w.gamma, w.steps_max, 1.0)
+        compared += int(np.sum(np.any(ids0 == w.mask_id, axis=1)))
+    final = (host(t["ids"]), host(t["steps"]), host(t["commit_step"]))
+    assert not np.any(final[0] == w.mask_id)
+    assert excluded <= max(2, compared // 2)  # the rest is checked for validity only
+    # the whole block in one graph launch reproduces the step-by-step result
+    t["ids"].fill_(w.mask_id)
+    t["n_masked"].fill_(S)
+    t["steps"].zero_()
+    t["commit_step"].zero_()
+    tt.tt_denoise_block_loop(desc, ts, ws)
+    torch.cuda.synchronize()
+    assert tt.tt_device_status(True) == 0
+    assert np.array_equal(host(t["ids"]), final[0])
+    assert np.array_equal(host(t["steps"]), final[1])
+    assert np.array_equal(host(t["commit_step"]), final[2])
