@@ -288,24 +288,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-__global__ void __launch_bounds__(32) lmhead_finish_kernel(LmHeadParams p) {
+// One CTA per sequence: warp w merges rows w, w + 8, ... (lanes stride over the row's
+// chunk partials, so all its loads are in flight together), then warp 0 decides.
+constexpr int kFinishThreads = 256;
+__global__ void __launch_bounds__(kFinishThreads) lmhead_finish_kernel(LmHeadParams p) {
     ttk::pdl_wait();  // the GEMM's partials (and, through it, the gather's dest[])
     ttk::pdl_trigger();
-    const int b = blockIdx.x, lane = threadIdx.x;
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const UnmaskParams& u = p.um;
     const Plan pl = make_plan(__ldcg(p.n_rows), p.V, p.n_ctas);
-    if (lane < u.S) {
-        const int row = b * u.S + lane;
+    for (int s = warp; s < u.S; s += kFinishThreads / 32) {
+        const int row = b * u.S + s;
         const int cr = __ldcg(p.dest + row);
-        if (cr >= 0) {
-            const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)cr * pl.n_chunks);
-            Red r{-CUDART_INF_F, 0.f, 0x7fffffff};
-            for (int c = 0; c < pl.n_chunks; ++c) r = combine(r, from_f4(__ldcg(pp + c)), u.temp_scale);
-            __stcg(reinterpret_cast<float4*>(u.row_res) + row, as_f4(r));
+        if (cr < 0) continue;  // warp-uniform
+        const float4* pp = reinterpret_cast<const float4*>(p.part + (size_t)cr * pl.n_chunks);
+        float4 v[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const int c = lane + 32 * i;
+            v[i] = (c < pl.n_chunks) ? __ldcg(pp + c) : make_float4(-CUDART_INF_F, 0.f, __int_as_float(0x7fffffff), 0.f);
         }
+        Red r = from_f4(v[0]);
+#pragma unroll
+        for (int i = 1; i < 5; ++i) r = combine(r, from_f4(v[i]), u.temp_scale);
+        for (int c = lane + 160; c < pl.n_chunks; c += 32) r = combine(r, from_f4(__ldcg(pp + c)), u.temp_scale);
+        r = warp_combine(r, u.temp_scale);
+        if (lane == 0) __stcg(reinterpret_cast<float4*>(u.row_res) + row, as_f4(r));
     }
-    __syncwarp();
-    decide(u, b);
+    __syncthreads();  // the row results are visible to warp 0
+    if (warp == 0) decide(u, b);
 }
 
 std::mutex g_attr_mu;
@@ -367,7 +378,7 @@ cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStr
     if (e != cudaSuccess) return e;
     e = launch_pdl(lmhead_gemm_kernel, dim3(p.n_ctas), dim3(kGemmThreads), (size_t)kSmemBytes, stream, maps, p);
     if (e != cudaSuccess) return e;
-    return launch_pdl(lmhead_finish_kernel, dim3(p.um.B), dim3(32), 0, stream, p);
+    return launch_pdl(lmhead_finish_kernel, dim3(p.um.B), dim3(kFinishThreads), 0, stream, p);
 }
 
 }  // namespace tti
