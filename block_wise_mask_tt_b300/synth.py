@@ -316,3 +316,11 @@ def make_lmhead_weights(w: Workload, seed: int = 0, rows: int = 8192) -> np.ndar
         v1 = min(V, v0 + rows)
         out[v0:v1] = _normal_bf16(r, (v1 - v0, H), sigma, 1.0)
     return out
+
+
+def make_qkv_weights(w: Workload, seed: int = 0) -> np.ndarray:
+    """bf16 fused projection [(Hq + 2 Hkv) D][H]: rows 0 .. Hq D - 1 make the queries
+    (head-major), then the keys, then the values.  N(0, 1/H), so unit-RMS hidden rows
+    give unit-variance q/k/v entries like the directly drawn workloads."""
+    n = (w.Hq + 2 * w.Hkv) * w.D
+    return _normal_bf16(_rng(seed, 32), (n, w.H), 1.0 / math.sqrt(w.H), 1.0)

@@ -17,7 +17,9 @@ Sources ("Nemotron-Labs-TwoTower" wiki page unless stated otherwise):
   "Block-wise generation" and "Release history and artifacts" and the opening summary;
 * the outer loop (block append, stopping) - section "Block-wise generation" and the
   MLX README's "Configuration (diffusion)";
-* the LM head that feeds the unmask step - section "Block-wise generation".
+* the LM head that feeds the unmask step - section "Block-wise generation";
+* the query/key/value projection of the adaLN output - sections "Motivation: one
+  network, two roles" and "Architecture".
 
 Every function computes the plain definition: no blocking, no fusion, no reordering
 beyond what the definition states.  Readings where the pages are silent are listed
@@ -30,6 +32,7 @@ from .loop import denoise_block, denoise_block_batch
 from .samplers import sampler_step, sampler_block, row_confidence_t
 from .outer import append_block, generate
 from .lmhead import lm_head_logits, lm_head_step
+from .qkv import qkv_projection
 
 __all__ = [
     "adaln_modulate",
@@ -47,4 +50,5 @@ __all__ = [
     "generate",
     "lm_head_logits",
     "lm_head_step",
+    "qkv_projection",
 ]

@@ -625,3 +625,40 @@ def check_lm_head_decoded_rows_unused(step_fn):
 LMHEAD_LOGIT_CHECKS = [check_lm_head_one_hot_rows, check_lm_head_vs_torch_linear]
 LMHEAD_STEP_CHECKS = [check_lm_head_scaled_basis_rows, check_lm_head_mask_row_never_emitted,
                       check_lm_head_decoded_rows_unused]
+
+
+# ----------------------------------------------------------------------------------
+# query/key/value projection of the adaLN output
+# ----------------------------------------------------------------------------------
+
+def check_qkv_one_hot_rows(proj_fn):
+    """Row r of W_qkv = e_{pi(r)} (exact ones): every output entry is one hidden component,
+    placed by the (q heads, k heads, v heads) x D column order."""
+    B, S, H, Hq, Hkv, D = 2, 3, 16, 4, 2, 8
+    n = (Hq + 2 * Hkv) * D
+    pi = np.random.default_rng(12).integers(0, H, n)
+    W = np.zeros((n, H), np.uint16)
+    W[np.arange(n), pi] = BF16_ONE
+    y = _rand_bf16(13, (B, S, H))
+    q, k, v = proj_fn(y, W, Hq, Hkv, D)
+    yf = synth.bf16_bits_to_f32(y).astype(np.float64)
+    for h in range(Hq):
+        for d in range(D):
+            assert np.array_equal(q[:, :, h, d], yf[:, :, pi[h * D + d]])
+    for h in range(Hkv):
+        for d in range(D):
+            assert np.array_equal(k[:, :, h, d], yf[:, :, pi[(Hq + h) * D + d]])
+            assert np.array_equal(v[:, :, h, d], yf[:, :, pi[(Hq + Hkv + h) * D + d]])
+
+
+def check_qkv_vs_torch_linear(proj_fn):
+    B, S, H, Hq, Hkv, D = 3, 5, 40, 4, 1, 16
+    y = _rand_bf16(14, (B, S, H))
+    W = _rand_bf16(15, ((Hq + 2 * Hkv) * D, H), 0.2)
+    q, k, v = proj_fn(y, W, Hq, Hkv, D)
+    full = F.linear(_bf(y), _bf(W)).numpy()
+    got = np.concatenate([q.reshape(B, S, -1), k.reshape(B, S, -1), v.reshape(B, S, -1)], axis=-1)
+    np.testing.assert_allclose(got, full, rtol=1e-12, atol=1e-12)
+
+
+QKV_CHECKS = [check_qkv_one_hot_rows, check_qkv_vs_torch_linear]
