@@ -65,6 +65,21 @@ __device__ __forceinline__ Plan make_plan(int n_rows, int V, int n_ctas) {
     return pl;
 }
 
+// One persistent GEMM, two epilogues: the LM head's softmax reduction (per-row chunk
+// partials) and the projection's bf16 store into up to three column segments.
+struct GemmArgs {
+    const int32_t* n_rows_dev;  // rows counted on the device, or null: n_rows
+    int n_rows;
+    int H, N;                   // reduction extent, output columns
+    int n_ctas;
+    UnmaskPartial* part;        // reduction: [rows][n_chunks]
+    float temp_scale;
+    int32_t mask_id;
+    uint16_t* out[3];           // store: column segments [0, c0), [c0, c0 + c1), [.., N)
+    int seg_cols[3];
+    int* err;
+};
+
 __global__ void __launch_bounds__(256) lmhead_gather_kernel(LmHeadParams p) {
     ttk::pdl_wait();
     ttk::pdl_trigger();
@@ -116,8 +131,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ttk::mbar_wait(bar, parity));
 }
 
+template <bool kStore>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    lmhead_gemm_kernel(const __grid_constant__ LmHeadMaps maps, const LmHeadParams p) {
+    gemm_kernel(const __grid_constant__ LmHeadMaps maps, const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -153,12 +169,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ttk::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    ttk::pdl_wait();  // the gather kernel's row count, dest[] and a_c
+    ttk::pdl_wait();  // the producer of A (gather or adaLN kernel) has completed
     ttk::pdl_trigger();
-    const int n_rows = __ldcg(p.n_rows);
-    const Plan pl = make_plan(n_rows, p.V, p.n_ctas);
+    const int n_rows = g.n_rows_dev ? __ldcg(g.n_rows_dev) : g.n_rows;
+    const Plan pl = make_plan(n_rows, g.N, g.n_ctas);
     const int items = pl.n_mt * pl.n_chunks;
-    const int nkb = (p.H + 63) / 64;
+    const int nkb = (g.H + 63) / 64;
     bool ok = true;
 
     // item -> (row tile, chunk, first and end unit of the chunk)
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
-            if (!ok) ttk::report_error(p.um.err, ttk::kErrTimeout);
+            if (!ok) ttk::report_error(g.err, ttk::kErrTimeout);
             // Drain: the loads of the most recent stages have landed before exit.
             for (uint32_t j = (kc > (uint32_t)kStages) ? kc - kStages : 0u; j < kc; ++j)
                 ttk::mbar_wait(full_bar(j % kStages), (j / kStages) & 1u);
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (ok) ttk::mma_commit(accf_bar(a));
                 }
             }
-            if (!ok) ttk::report_error(p.um.err, ttk::kErrTimeout);
+            if (!ok) ttk::report_error(g.err, ttk::kErrTimeout);
             // Everything issued has completed before shared memory and TMEM are released.
             ttk::mma_commit(done_bar);
             ttk::mbar_wait(done_bar, 0);
@@ -239,13 +255,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int quarter = warp & 3;  // warps 2, 3, 4, 5 -> TMEM lanes 64, 96, 0, 32
         const int lane_row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const float ts = p.um.temp_scale;
-        const int mask = p.um.mask_id;
         uint32_t it = 0;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
             int mt, chunk, u0, u1;
             item_geom(item, mt, chunk, u0, u1);
-            const int vend = min(p.V, u1 * 64);
+            const int vend = min(g.N, u1 * 64);
+            const int row = mt * 128 + lane_row;
             Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
             for (int ut = u0; ut < u1; ut += 4, ++it) {
                 const uint32_t a = it & 1u;
@@ -260,25 +275,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t r[32];
                     ttk::tmem_ld32(tmem + lane_off + a * 256u + 32u * c, r);
                     ttk::tmem_ld_wait32(r);
-                    float x[32];
-                    int id[32];
+                    const int col0 = v + 32 * c;
+                    if constexpr (kStore) {
+                        // 32 columns lie in one segment (segment widths are multiples of 64)
+                        if (row < n_rows && col0 < vend) {
+                            const int c01 = g.seg_cols[0] + g.seg_cols[1];
+                            uint16_t* base = (col0 < g.seg_cols[0]) ? g.out[0] : (col0 < c01) ? g.out[1] : g.out[2];
+                            const int width = (col0 < g.seg_cols[0]) ? g.seg_cols[0] : (col0 < c01) ? g.seg_cols[1] : g.seg_cols[2];
+                            const int c_in = col0 - ((col0 < g.seg_cols[0]) ? 0 : (col0 < c01) ? g.seg_cols[0] : c01);
+                            uint4* dst = reinterpret_cast<uint4*>(base + (size_t)row * width + c_in);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int col = v + 32 * c + e;
-                        id[e] = col;
-                        x[e] = (col < vend && col != mask) ? __uint_as_float(r[e]) : -CUDART_INF_F;
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                                        __uint_as_float(r[8 * q4 + 2 * u]), __uint_as_float(r[8 * q4 + 2 * u + 1]));
+                                    w[u] = *reinterpret_cast<const uint32_t*>(&pr);
+                                }
+                                dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    } else {
+                        float x[32];
+                        int id[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int col = col0 + e;
+                            id[e] = col;
+                            x[e] = (col < vend && col != g.mask_id) ? __uint_as_float(r[e]) : -CUDART_INF_F;
+                        }
+                        fold<32>(acc, x, id, g.temp_scale);
                     }
-                    fold<32>(acc, x, id, ts);
                 }
                 ttk::tc_fence_before();
                 ttk::mbar_arrive(acce_bar(a));
             }
             if (!ok) break;
-            const int cr = mt * 128 + lane_row;
-            if (cr < n_rows)
-                __stcg(reinterpret_cast<float4*>(p.part + (size_t)cr * pl.n_chunks + chunk), as_f4(acc));
+            if constexpr (!kStore) {
+                if (row < n_rows)
+                    __stcg(reinterpret_cast<float4*>(g.part + (size_t)row * pl.n_chunks + chunk), as_f4(acc));
+            }
         }
-        if (!ok) ttk::report_error(p.um.err, ttk::kErrTimeout);
+        if (!ok) ttk::report_error(g.err, ttk::kErrTimeout);
     }
     ttk::tc_fence_before();
     __syncthreads();
@@ -328,7 +367,9 @@ cudaError_t gemm_prepare() {
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (dev >= 0 && dev < 64 && ((g_attr_done >> dev) & 1ull)) return cudaSuccess;
-    e = cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64) g_attr_done |= (1ull << dev);
     return e;
 }
@@ -376,9 +417,39 @@ cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStr
     const int n_gather = (p.rows + kGatherRows - 1) / kGatherRows;
     e = launch_pdl(lmhead_gather_kernel, dim3(n_gather), dim3(256), 0, stream, p);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(lmhead_gemm_kernel, dim3(p.n_ctas), dim3(kGemmThreads), (size_t)kSmemBytes, stream, maps, p);
+    GemmArgs g{};
+    g.n_rows_dev = p.n_rows;
+    g.n_rows = 0;
+    g.H = p.H;
+    g.N = p.V;
+    g.n_ctas = p.n_ctas;
+    g.part = p.part;
+    g.temp_scale = p.um.temp_scale;
+    g.mask_id = p.um.mask_id;
+    g.err = p.um.err;
+    e = launch_pdl(gemm_kernel<false>, dim3(p.n_ctas), dim3(kGemmThreads), (size_t)kSmemBytes, stream, maps, g);
     if (e != cudaSuccess) return e;
     return launch_pdl(lmhead_finish_kernel, dim3(p.um.B), dim3(kFinishThreads), 0, stream, p);
+}
+
+cudaError_t launch_qkv(const QkvParams& p, const LmHeadMaps& maps, cudaStream_t stream) {
+    cudaError_t e = gemm_prepare();
+    if (e != cudaSuccess) return e;
+    GemmArgs g{};
+    g.n_rows_dev = nullptr;
+    g.n_rows = p.rows;
+    g.H = p.H;
+    g.N = (p.Hq + 2 * p.Hkv) * p.D;
+    g.n_ctas = p.n_ctas;
+    g.mask_id = -1;
+    g.out[0] = p.q;
+    g.out[1] = p.k;
+    g.out[2] = p.v;
+    g.seg_cols[0] = p.Hq * p.D;
+    g.seg_cols[1] = p.Hkv * p.D;
+    g.seg_cols[2] = p.Hkv * p.D;
+    g.err = p.err;
+    return launch_pdl(gemm_kernel<true>, dim3(p.n_ctas), dim3(kGemmThreads), (size_t)kSmemBytes, stream, maps, g);
 }
 
 }  // namespace tti

@@ -352,6 +352,47 @@ tt_status enqueue_lmhead(const void* hidden, const void* w_vocab, int32_t* ids, 
     return TT_OK;
 }
 
+tt_status check_qkv(int B, int S, int H, int Hq, int Hkv, int D) {
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+        return fail(TT_ERR_INVALID_ARG, "B, S, Hq, Hkv must be >= 1 and Hkv must divide Hq");
+    if (D != 64 && D != 128) return fail(TT_ERR_UNSUPPORTED, "D must be 64 or 128");
+    if (H < 64 || H % 8 != 0) return fail(TT_ERR_UNSUPPORTED, "H must be a multiple of 8, at least 64");
+    if ((long long)B * S > 65535LL * 128) return fail(TT_ERR_UNSUPPORTED, "B*S too large");
+    return TT_OK;
+}
+
+tt_status enqueue_qkv(const void* y, const void* w_qkv, void* q, void* k, void* v, int B, int S, int H,
+                      int Hq, int Hkv, int D, int* err, cudaStream_t st) {
+    int n_ctas = 0;
+    TT_TRY(sm_count(&n_ctas));
+    tti::QkvParams p{};
+    p.q = static_cast<uint16_t*>(q);
+    p.k = static_cast<uint16_t*>(k);
+    p.v = static_cast<uint16_t*>(v);
+    p.rows = B * S;
+    p.H = H;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.D = D;
+    p.n_ctas = n_ctas;
+    p.err = err;
+    tti::LmHeadMaps maps;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)p.rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t box[2] = {64, 128};
+        TT_TRY(encode_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box));
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)(Hq + 2 * Hkv) * D};
+        const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t box[2] = {64, 64};
+        TT_TRY(encode_map(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_qkv, dims, strides, box));
+    }
+    TT_CUDA(tti::launch_qkv(p, maps, st));
+    return TT_OK;
+}
+
 // ------------------------------------------------------------- step (shared pieces)
 struct StepPlan {
     AttnPlan attn;
@@ -378,6 +419,9 @@ tt_status plan_step(const tt_step_desc* d, StepPlan& sp) {
         return fail(TT_ERR_INVALID_ARG, "sampler must be a tt_sampler_kind");
     if (!(d->temperature > 0.f) || !(d->temperature < 1e30f))
         return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
+    if (d->qkv_proj != 0 && d->qkv_proj != 1) return fail(TT_ERR_INVALID_ARG, "qkv_proj must be 0 or 1");
+    if (d->qkv_proj)
+        TT_TRY(check_qkv(d->attn.B, d->attn.S, d->H, d->attn.Hq, d->attn.Hkv, d->attn.D));
     sp.lm_head = d->logits.kind == TT_LOGITS_LM_HEAD;
     sp.n_ctas = 0;
     size_t tail_ws = 0;
@@ -412,6 +456,15 @@ tt_status check_step_tensors(const tt_step_desc* d, const tt_step_tensors* t) {
         TT_TRY(need_ptr(t->logits, "logits"));
     }
     if (t->y == t->x) return fail(TT_ERR_INVALID_ARG, "y may not alias x");
+    if (d->qkv_proj) {
+        TT_TRY(need_ptr(t->w_qkv, "w_qkv"));
+        TT_TRY(need_ptr(t->q, "q"));
+        TT_TRY(need_ptr(t->k_blk, "k_blk"));
+        TT_TRY(need_ptr(t->v_blk, "v_blk"));
+        TT_CUDA(tti::lmhead_prepare());
+        int n = 0;
+        TT_TRY(sm_count(&n));  // cached before any graph capture
+    }
     return TT_OK;
 }
 
@@ -434,6 +487,11 @@ tt_status enqueue_step(const tt_step_desc* d, const tt_step_tensors* t, const St
     ap.eps = d->ln_eps;
     ap.err = err;
     TT_CUDA(tti::launch_adaln(ap, st));
+
+    if (d->qkv_proj)  // q, k_blk, v_blk are this step's projections of y
+        TT_TRY(enqueue_qkv(t->y, t->w_qkv, const_cast<void*>(t->q), const_cast<void*>(t->k_blk),
+                           const_cast<void*>(t->v_blk), B, S, d->H, d->attn.Hq, d->attn.Hkv, d->attn.D,
+                           err, st));
 
     TT_TRY(launch_attention(sp.attn, t->q, t->k_blk, t->v_blk, t->page_table, t->ctx_len,
                             t->n_masked, t->attn_out, nullptr, ws, err, st));
@@ -1010,6 +1068,19 @@ tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32_t* ids
     return enqueue_lmhead(hidden, w_vocab, ids, n_masked, steps, conf, commit, commit_step, B, S, H, V,
                           mask_id, sampler->kind, sampler->gamma, sampler->max_steps, sampler->temperature,
                           n_ctas, workspace, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tt_status tt_qkv_project(const void* y, const void* w_qkv, void* q, void* k_blk, void* v_blk, int B, int S,
+                         int H, int Hq, int Hkv, int D, tt_stream_t stream) {
+    TT_TRY(check_qkv(B, S, H, Hq, Hkv, D));
+    TT_TRY(need_ptr(y, "y"));
+    TT_TRY(need_ptr(w_qkv, "w_qkv"));
+    TT_TRY(need_ptr(q, "q"));
+    TT_TRY(need_ptr(k_blk, "k_blk"));
+    TT_TRY(need_ptr(v_blk, "v_blk"));
+    int* err = nullptr;
+    TT_TRY(device_err_word(&err));
+    return enqueue_qkv(y, w_qkv, q, k_blk, v_blk, B, S, H, Hq, Hkv, D, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -128,6 +128,17 @@ void lmhead_layout(void* ws, LmHeadParams& p);
 cudaError_t launch_lmhead(const LmHeadParams& p, const LmHeadMaps& maps, cudaStream_t stream);
 cudaError_t lmhead_prepare();  // sets the GEMM's shared-memory limit on this device
 
+// Query/key/value projection of the adaLN output on the same persistent GEMM: y [rows][H]
+// times W_qkv [(Hq + 2 Hkv) D][H]^T, rounded to bf16 and stored into q [rows][Hq D],
+// k [rows][Hkv D], v [rows][Hkv D].  maps.a covers y (box 64 x 128), maps.w W_qkv.
+struct QkvParams {
+    uint16_t *q, *k, *v;
+    int rows, H, Hq, Hkv, D;
+    int n_ctas;
+    int* err;
+};
+cudaError_t launch_qkv(const QkvParams& p, const LmHeadMaps& maps, cudaStream_t stream);
+
 // -------------------------------------------------------------------------- attention
 struct AttnGeom {
     int B, S, Hq, Hkv, G, D;

@@ -54,7 +54,7 @@ class tt_step_desc(ctypes.Structure):
                 ("mask_id", ctypes.c_int32), ("gamma", ctypes.c_float),
                 ("max_steps", ctypes.c_int), ("ln_eps", ctypes.c_float),
                 ("logits", tt_logits_spec), ("sampler", ctypes.c_int),
-                ("temperature", ctypes.c_float)]
+                ("temperature", ctypes.c_float), ("qkv_proj", ctypes.c_int)]
 
 
 SAMPLER_CONFIDENCE, SAMPLER_MOCK_AR, SAMPLER_PREDICT_NOISE = 0, 1, 2
@@ -72,7 +72,7 @@ class tt_sampler(ctypes.Structure):
 
 _STEP_TENSOR_FIELDS = ("x", "shift_table", "scale_table", "q", "k_blk", "v_blk", "k_ctx", "v_ctx",
                        "page_table", "ctx_len", "ids", "n_masked", "steps", "commit_step", "y",
-                       "attn_out", "logits", "conf", "commit", "w_vocab")
+                       "attn_out", "logits", "conf", "commit", "w_vocab", "w_qkv")
 
 
 class tt_step_tensors(ctypes.Structure):
@@ -102,6 +102,7 @@ _SIGS = {
     "tt_lmhead_unmask_workspace": (ctypes.c_size_t, [_I, _I, _I]),
     "tt_lmhead_unmask": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_int32,
                               ctypes.POINTER(tt_sampler), _P, ctypes.c_size_t, _P]),
+    "tt_qkv_project": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "tt_denoise_workspace": (ctypes.c_size_t, [ctypes.POINTER(tt_step_desc)]),
     "tt_append_block": (_I, [ctypes.POINTER(tt_attn_dims), _P, _P, _P, _P, _P, _P, _P,
                              ctypes.POINTER(tt_stop_spec), _P, _P, _P, _I, _I, _P]),
@@ -241,6 +242,13 @@ def tt_sampler_unmask(logits, ids, steps, B, S, V, mask_id, sampler: tt_sampler,
         ctypes.byref(sampler), ws.data_ptr(), ws.numel(), _stream(stream)))
 
 
+def tt_qkv_project(y, w_qkv, q, k_blk, v_blk, B, S, H, Hq, Hkv, D, stream=None) -> None:
+    _check(lib.tt_qkv_project(
+        _ptr(y, "y", _BF16, B * S * H), _ptr(w_qkv, "w_qkv", _BF16, (Hq + 2 * Hkv) * D * H),
+        _ptr(q, "q", _BF16, B * S * Hq * D), _ptr(k_blk, "k_blk", _BF16, B * S * Hkv * D),
+        _ptr(v_blk, "v_blk", _BF16, B * S * Hkv * D), B, S, H, Hq, Hkv, D, _stream(stream)))
+
+
 def tt_lmhead_unmask_workspace(B, S, H) -> int:
     return int(lib.tt_lmhead_unmask_workspace(B, S, H))
 
@@ -274,10 +282,11 @@ def tt_confidence_unmask_noalloc(logits, ids, steps, B, S, V, mask_id, gamma, ma
 
 def step_desc(attn: tt_attn_dims, H, V, mask_id, gamma, max_steps, ln_eps, seed, block_index,
               kind, boost_lo, boost_hi, sampler: int = SAMPLER_CONFIDENCE,
-              temperature: float = 1.0) -> tt_step_desc:
+              temperature: float = 1.0, qkv_proj: bool = False) -> tt_step_desc:
     return tt_step_desc(attn, H, V, mask_id, float(gamma), max_steps, float(ln_eps),
                         tt_logits_spec(seed & 0xFFFFFFFF, block_index, kind, float(boost_lo),
-                                       float(boost_hi)), int(sampler), float(temperature))
+                                       float(boost_hi)), int(sampler), float(temperature),
+                        1 if qkv_proj else 0)
 
 
 def step_tensors(**tensors) -> tt_step_tensors:

@@ -284,6 +284,25 @@ TT_API tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32
                                   void* workspace, size_t workspace_bytes, tt_stream_t stream);
 
 /* --------------------------------------------------------------------------------
+ * tt_qkv_project: the denoiser's query/key/value projection of the adaLN output.
+ *
+ * "Nemotron-Labs-TwoTower" wiki, "Motivation: one network, two roles" (the denoiser
+ * is conditioned on the timestep through adaptive layer normalisation) and
+ * "Architecture" (the block's queries and its own keys/values are the denoiser's
+ * projections; the block attends over the context cache followed by them).
+ *   out[r][c] = sum_k y[r][k] * w_qkv[c][k]   (fp32 accumulation, bf16 RNE store)
+ * for r = b*S + s; column c < Hq*D goes to q[b][s][c / D][c % D], the next Hkv*D
+ * columns to k_blk, the last Hkv*D to v_blk.
+ *   y      bf16 [B][S][H], device, 16-byte aligned
+ *   w_qkv  bf16 [(Hq + 2 Hkv) D][H], device, 16-byte aligned
+ *   q      bf16 [B][S][Hq][D] (out); k_blk, v_blk bf16 [B][S][Hkv][D] (out)
+ * Limits: D in {64, 128}, Hkv divides Hq, H a multiple of 8 and >= 64.  One
+ * persistent tcgen05 GEMM kernel on `stream`; no workspace.
+ * -------------------------------------------------------------------------------- */
+TT_API tt_status tt_qkv_project(const void* y, const void* w_qkv, void* q, void* k_blk, void* v_blk,
+                                int B, int S, int H, int Hq, int Hkv, int D, tt_stream_t stream);
+
+/* --------------------------------------------------------------------------------
  * tt_confidence_unmask_noalloc: the same confidence-unmasking step, for callers that
  * cannot provide a workspace.  The pages describing the method have no counterpart
  * to this entry point; it exists for callers whose device memory is owned entirely
@@ -324,6 +343,8 @@ TT_API tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids,
  * One step, for every sequence that still has masked positions:
  *   adaLN(x, table row n_masked[b]) -> y; attention -> attn_out; synthetic logits
  *   for the masked rows (step index steps[b]) -> logits; confidence unmasking.
+ * With qkv_proj = 1 the step first projects y into q, k_blk and v_blk
+ * (tt_qkv_project with t->w_qkv), so the attention's inputs depend on t.
  * With logits.kind == TT_LOGITS_LM_HEAD the last two are replaced by the fused LM
  * head and sampler step of tt_lmhead_unmask with hidden = y and W = t->w_vocab (no
  * logits buffer is used; H >= 64, V >= 64, B*S <= 4096).
@@ -341,6 +362,7 @@ typedef struct {
     tt_logits_spec logits;
     int sampler;            /* tt_sampler_kind: TT_SAMPLER_CONFIDENCE (0) for the main sampler */
     float temperature;      /* > 0; 1 = plain softmax */
+    int qkv_proj;           /* 1: q, k_blk, v_blk = tt_qkv_project(y, w_qkv) every step */
 } tt_step_desc;
 
 typedef struct {
@@ -368,6 +390,8 @@ typedef struct {
     uint8_t* commit;            /* uint8 [B][S] or NULL                     */
     /* LM head (logits.kind == TT_LOGITS_LM_HEAD), else NULL */
     const void* w_vocab;        /* bf16 [V][H]                              */
+    /* projection (qkv_proj == 1), else NULL; q, k_blk, v_blk are then written */
+    const void* w_qkv;          /* bf16 [(Hq + 2 Hkv) D][H]                 */
 } tt_step_tensors;
 
 /* Workspace for tt_denoise_step / tt_denoise_block_loop (attention partials, unmask
