@@ -66,6 +66,11 @@ def parse_args():
     ap.add_argument("--lm-head", action="store_true",
                     help="the step's logits come from the fused LM head over the adaLN output "
                          "(synthetic projection W [V][H]) instead of the hash stand-in")
+    ap.add_argument("--qkv-proj", action="store_true",
+                    help="every step projects the adaLN output into q, k_blk, v_blk (synthetic "
+                         "W_qkv) before the attention, so they follow the timestep")
+    ap.add_argument("--no-qkv-leg", action="store_true",
+                    help="skip the standalone timing of the query/key/value projection")
     ap.add_argument("--no-lm-head-leg", action="store_true",
                     help="skip the standalone timing of the fused LM head + sampler step")
     ap.add_argument("--generate", type=int, default=32,
@@ -202,13 +207,15 @@ class Workbench:
     """Device-resident inputs, state and buffers for one replica of the workload."""
 
     def __init__(self, tt, torch, w: synth.Workload, seed: int, sampler: int = 0,
-                 temperature: float = 1.0, lm_head: bool = False):
+                 temperature: float = 1.0, lm_head: bool = False, qkv_proj: bool = False):
         self.tt, self.torch, self.w, self.seed = tt, torch, w, seed
         self.lm_head = lm_head
+        self.qkv_proj = qkv_proj
         t0 = time.time()
         self.inp = synth.make_attention_inputs(w, seed)
         self.ad = synth.make_adaln_inputs(w, seed)
         self.w_vocab = self._dev(synth.make_lmhead_weights(w, seed)) if lm_head else None
+        self.w_qkv = self._dev(synth.make_qkv_weights(w, seed)) if qkv_proj else None
         self.gen_s = time.time() - t0
         B, S = w.B, w.S
         dev = lambda a: self._dev(a)
@@ -236,11 +243,11 @@ class Workbench:
             logits=None if lm_head else T.empty((B, S, w.V), dtype=T.float32, device="cuda"),
             conf=T.empty((B, S), dtype=T.float32, device="cuda"),
             commit=T.empty((B, S), dtype=T.uint8, device="cuda"),
-            w_vocab=self.w_vocab)
+            w_vocab=self.w_vocab, w_qkv=self.w_qkv)
         kind = tt.LOGITS_LM_HEAD if lm_head else w.logits_kind
         self.desc = tt.step_desc(self.dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps,
                                  seed, 0, kind, w.boost_lo, w.boost_hi, sampler=sampler,
-                                 temperature=temperature)
+                                 temperature=temperature, qkv_proj=qkv_proj)
         self.ts = tt.step_tensors(**self.t)
         self.ws = tt.workspace(tt.tt_denoise_workspace(self.desc))
         ctx = self.inp["ctx_len"].astype(np.int64)
@@ -296,7 +303,8 @@ def run_timed(wb: Workbench, plan, flush, with_events=True):
         wb.reset()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        per_step = 6 if wb.lm_head else 5  # adaLN, split, merge, then logits + unmask or the LM head's 3
+        # adaLN, [projection], split, merge, then logits + unmask or the LM head's 3 kernels
+        per_step = (6 if wb.lm_head else 5) + (1 if wb.qkv_proj else 0)
         if take == n:
             wb.block(bi)
             launches += 2 + (per_step + 1) * n  # dyn-slot write + count, then the step and loop_cond
@@ -402,6 +410,45 @@ def run_lmhead(wb: Workbench, flush, reps: int = 5):
             "TFLOP_s": flops / t / 1e12, "GB_s": byts / t / 1e9,
             "roofline_us": max(flops / (tc * 1e12), byts / (hbm * 1e9)) * 1e6,
             "call": "tt_lmhead_unmask, every row masked (first step of a block), L2 flushed"}
+
+
+def run_qkv(wb: Workbench, flush, reps: int = 5):
+    """Standalone tt_qkv_project calls on the workload's shape (every position), L2
+    flushed before each; returns the leg's dict with its roofline."""
+    tt, torch, w = wb.tt, wb.torch, wb.w
+    B, S, N = w.B, w.S, (w.Hq + 2 * w.Hkv) * w.D
+    W = wb.w_qkv if wb.w_qkv is not None else wb._dev(synth.make_qkv_weights(w, wb.seed))
+    y = wb._dev(synth.make_hidden(w, wb.seed))
+    q = torch.empty((B, S, w.Hq, w.D), dtype=torch.int16, device="cuda")
+    k = torch.empty((B, S, w.Hkv, w.D), dtype=torch.int16, device="cuda")
+    v = torch.empty_like(k)
+    stream = torch.cuda.current_stream()
+    ts = []
+    for r in range(reps + 2):
+        flush()
+        torch.cuda._sleep(200_000)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        tt.tt_qkv_project(y, W, q, k, v, B, S, w.H, w.Hq, w.Hkv, w.D)
+        e.record(stream)
+        e.synchronize()
+        if r >= 2:
+            ts.append(s.elapsed_time(e) / 1e3)
+    if tt.tt_device_status(True) != 0:
+        raise RuntimeError("device-side error reported by tt_qkv_project")
+    t = statistics.mean(ts)
+    flops = 2.0 * B * S * w.H * N
+    byts = float(N * w.H * 2 + B * S * (w.H + N) * 2)  # W, y read once; q/k/v written once
+    peaks, kind = load_peaks()
+    tc, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    bound = "tensor" if flops / (tc * 1e12) >= byts / (hbm * 1e9) else "hbm"
+    achieved = flops / t / 1e12 if bound == "tensor" else byts / t / 1e9
+    peak = tc if bound == "tensor" else hbm
+    return {"us": t * 1e6, "rows": B * S, "N": N, "H": w.H, "flops": flops, "algorithmic_bytes": byts,
+            "bound": bound, "achieved": achieved, "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+            "peak": peak, "frac": achieved / peak, "peak_source": kind,
+            "roofline_us": max(flops / (tc * 1e12), byts / (hbm * 1e9)) * 1e6,
+            "call": "tt_qkv_project over every position, L2 flushed"}
 
 
 def kernel_only(wb: Workbench, which: str, reps: int):
@@ -516,7 +563,7 @@ def run_generate(wb: Workbench, n_blocks: int, flush, reps: int = 3):
     dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, cap, 0, 0, 0, w.softmax_scale, 0)
     desc = tt.step_desc(dims, w.H, w.V, w.mask_id, w.gamma, w.steps_max, w.ln_eps, wb.seed, 0,
                         wb.desc.logits.kind, w.boost_lo, w.boost_hi, sampler=wb.desc.sampler,
-                        temperature=wb.desc.temperature)
+                        temperature=wb.desc.temperature, qkv_proj=bool(wb.desc.qkv_proj))
     t = dict(wb.t)
     t.update(k_ctx=kc, v_ctx=vc, ctx_len=ctx0.clone())
     ts = tt.step_tensors(**t)
@@ -679,7 +726,8 @@ def main():
 
     w = workload(args)
     seed = replica_seed(args.seed, rank)
-    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head)
+    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
+                   args.qkv_proj)
     if args.kernel_only:
         kernel_only(wb, args.kernel_only, args.reps)
         return
@@ -737,6 +785,10 @@ def main():
     if lm is not None:
         kernels["tt_lmhead_unmask"] = {k: lm[k] for k in ("us", "TFLOP_s", "GB_s", "bound", "roofline_us",
                                                            "frac", "algorithmic_bytes", "flops")}
+    qkv = None if args.no_qkv_leg and not args.qkv_proj else run_qkv(wb, flush)
+    if qkv is not None:
+        kernels["tt_qkv_project"] = {k: qkv[k] for k in ("us", "bound", "roofline_us", "frac",
+                                                        "algorithmic_bytes", "flops")}
     if args.lm_head:
         dominant = "attn" if ktimes["attn"] >= lm["us"] * 1e-6 else "lmhead"
     else:
@@ -790,6 +842,8 @@ def main():
                    "bench_step": "one denoise step of the whole batch",
                    "logits": ("fused LM head over the adaLN output (synthetic W [V][H], resident)"
                               if args.lm_head else "hash stand-in"),
+                   "qkv": ("projected from the adaLN output every step (synthetic W_qkv, resident)"
+                           if args.qkv_proj else "fixed synthetic tensors"),
                    "sampler": args.sampler, "temperature": args.temperature,
                    "blocks_timed": len(plan), "whole_blocks": blocks_full,
                    "tokens_per_step": w.B * w.S * blocks_full / max(1, sum(t for _, n, t in plan if t == n)),
@@ -803,6 +857,7 @@ def main():
         "clocks": clk.summary(),
         "generate": gen_line,
         "lm_head": lm,
+        "qkv_proj": qkv,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
