@@ -14,7 +14,8 @@
 //     a_c, vocabulary chunk); the chunks split the vocabulary in 64-id units so that
 //     items = row tiles x chunks covers the CTAs once.  Per 256-id vocabulary tile:
 //     warp 0 streams the A tile (128 rows x 64 of H) and four 64-row boxes of W per
-//     64-wide slice of H into a four-stage ring (TMA, 128-byte swizzle); warp 1 issues
+//     64-wide slice of H into a four-stage ring (TMA, 128-byte swizzle; narrower
+//     problems use tiles of one to three boxes and up to eight stages); warp 1 issues
 //     tcgen05.mma 128 x 256 x 16 into one of two TMEM accumulators (256 columns each,
 //     so the epilogue of one tile overlaps the products of the next); warps 2-5 (one
 //     TMEM lane = one row per thread) read the accumulator and fold it into the row's
@@ -39,16 +40,14 @@ namespace {
 
 using namespace um;
 
-constexpr int kStages = 4;
 constexpr uint32_t kATile = 128 * 128;                  // 128 rows x 64 bf16
 constexpr uint32_t kBBox = 64 * 128;                    // 64 vocabulary rows x 64 bf16
-constexpr uint32_t kBTile = 4 * kBBox;                  // 256 vocabulary rows
-constexpr uint32_t kStage = kATile + kBTile;            // 48 KiB
-constexpr uint32_t kBarOff = kStages * kStage;          // barriers after the ring
-constexpr uint32_t kSlotOff = kBarOff + 128;            // TMEM address slot
-constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t kRingBytes = 4 * (kATile + 4 * kBBox);  // four stages of the widest tile
+constexpr int kMaxStages = 8;
+constexpr uint32_t kBarOff = kRingBytes;                // barriers after the ring
+constexpr uint32_t kSlotOff = kBarOff + 256;            // TMEM address slot
+constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;   // + slack for 1024-B alignment
 constexpr int kGemmThreads = 192;                       // producer, MMA, 4 epilogue warps
-constexpr uint32_t kIdesc = ttk::idesc_bf16(128, 256, false, false);
 constexpr int kGatherRows = 8;                          // rows copied per gather CTA (one per warp)
 
 // Work split shared by the GEMM and the finish kernel.
@@ -140,10 +139,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t sbase = ttk::smem_u32(smem);
     const uint32_t bar0 = sbase + kBarOff;
     auto full_bar = [&](uint32_t st) { return bar0 + 8u * st; };
-    auto empty_bar = [&](uint32_t st) { return bar0 + 8u * (kStages + st); };
-    auto accf_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + a); };
-    auto acce_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
+    auto empty_bar = [&](uint32_t st) { return bar0 + 8u * (kMaxStages + st); };
+    auto accf_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kMaxStages + a); };
+    auto acce_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kMaxStages + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kMaxStages + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
 
     if (warp == 1) {
@@ -151,7 +150,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ttk::tmem_relinquish();
     }
     if (tid == 0) {
-        for (uint32_t st = 0; st < kStages; ++st) {
+        for (uint32_t st = 0; st < kMaxStages; ++st) {
             ttk::mbar_init(full_bar(st), 1);
             ttk::mbar_init(empty_bar(st), 1);
         }
@@ -175,6 +174,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const Plan pl = make_plan(n_rows, g.N, g.n_ctas);
     const int items = pl.n_mt * pl.n_chunks;
     const int nkb = (g.H + 63) / 64;
+    // Vocabulary tiles are wbox 64-id units wide (the widest chunk needs no more); the
+    // ring then holds as many stages of A + wbox boxes as fit, up to eight, so narrow
+    // problems keep more k-slices in flight.
+    const int wbox = pl.n_chunks ? min(4, (pl.units + pl.n_chunks - 1) / pl.n_chunks) : 4;
+    const uint32_t stage_bytes = kATile + (uint32_t)wbox * kBBox;
+    const uint32_t n_stages = min((uint32_t)kMaxStages, kRingBytes / stage_bytes);
+    const uint32_t idesc = ttk::idesc_bf16(128, 64 * wbox, false, false);
     bool ok = true;
 
     // item -> (row tile, chunk, first and end unit of the chunk)
@@ -188,59 +194,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t kc = 0;
+            uint32_t kc = 0, st = 0, ph = 0;  // k-slices issued; ring slot and lap parity
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
                 int mt, chunk, u0, u1;
                 item_geom(item, mt, chunk, u0, u1);
-                for (int ut = u0; ut < u1 && ok; ut += 4) {
-                    const int nbox = min(4, u1 - ut);
+                for (int ut = u0; ut < u1 && ok; ut += wbox) {
+                    const int nbox = min(wbox, u1 - ut);
                     for (int kb = 0; kb < nkb; ++kb, ++kc) {
-                        const uint32_t st = kc % kStages;
-                        if (kc >= (uint32_t)kStages && !ttk::mbar_wait(empty_bar(st), ((kc / kStages) - 1) & 1u)) {
+                        if (kc >= n_stages && !ttk::mbar_wait(empty_bar(st), ph ^ 1u)) {
                             ok = false;
                             break;
                         }
-                        const uint32_t sA = sbase + st * kStage, sB = sA + kATile;
+                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + kATile;
                         ttk::mbar_arrive_expect_tx(full_bar(st), kATile + (uint32_t)nbox * kBBox);
                         ttk::tma_load_2d(sA, &maps.a, kb * 64, mt * 128, full_bar(st));
                         for (int i = 0; i < nbox; ++i)
                             ttk::tma_load_2d(sB + (uint32_t)i * kBBox, &maps.w, kb * 64, (ut + i) * 64, full_bar(st));
+                        if (++st == n_stages) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                 }
             }
             if (!ok) ttk::report_error(g.err, ttk::kErrTimeout);
             // Drain: the loads of the most recent stages have landed before exit.
-            for (uint32_t j = (kc > (uint32_t)kStages) ? kc - kStages : 0u; j < kc; ++j)
-                ttk::mbar_wait(full_bar(j % kStages), (j / kStages) & 1u);
+            for (uint32_t j = (kc > n_stages) ? kc - n_stages : 0u; j < kc; ++j)
+                ttk::mbar_wait(full_bar(j % n_stages), (j / n_stages) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t kc = 0, it = 0;
+            uint32_t it = 0, st = 0, ph = 0;  // ring slot and lap parity
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
                 int mt, chunk, u0, u1;
                 item_geom(item, mt, chunk, u0, u1);
-                for (int ut = u0; ut < u1 && ok; ut += 4, ++it) {
+                for (int ut = u0; ut < u1 && ok; ut += wbox, ++it) {
                     const uint32_t a = it & 1u;
                     if (it >= 2 && !ttk::mbar_wait(acce_bar(a), ((it >> 1) - 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     ttk::tc_fence_after();
-                    for (int kb = 0; kb < nkb; ++kb, ++kc) {
-                        const uint32_t st = kc % kStages;
-                        if (!ttk::mbar_wait(full_bar(st), (kc / kStages) & 1u)) {
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!ttk::mbar_wait(full_bar(st), ph)) {
                             ok = false;
                             break;
                         }
                         ttk::tc_fence_after();
-                        const uint32_t sA = sbase + st * kStage, sB = sA + kATile;
+                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + kATile;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             ttk::mma_bf16_ss(tmem + a * 256u, ttk::sdesc_sw128(sA + 32u * k, 16, 1024),
-                                             ttk::sdesc_sw128(sB + 32u * k, 16, 1024), kIdesc,
+                                             ttk::sdesc_sw128(sB + 32u * k, 16, 1024), idesc,
                                              (kb > 0 || k > 0) ? 1u : 0u);
                         ttk::mma_commit(empty_bar(st));  // this stage is no longer read
+                        if (++st == n_stages) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                     if (ok) ttk::mma_commit(accf_bar(a));
                 }
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int vend = min(g.N, u1 * 64);
             const int row = mt * 128 + lane_row;
             Red acc{-CUDART_INF_F, 0.f, 0x7fffffff};
-            for (int ut = u0; ut < u1; ut += 4, ++it) {
+            for (int ut = u0; ut < u1; ut += wbox, ++it) {
                 const uint32_t a = it & 1u;
                 if (!warp_wait(accf_bar(a), (it >> 1) & 1u)) {
                     ok = false;
@@ -271,7 +283,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 ttk::tc_fence_after();
                 const int v = ut * 64;
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 2 * wbox; ++c) {
                     uint32_t r[32];
                     ttk::tmem_ld32(tmem + lane_off + a * 256u + 32u * c, r);
                     ttk::tmem_ld_wait32(r);
