@@ -153,3 +153,55 @@ def test_split_count_and_workspace_scale():
     small = tt.tt_denoise_attn_workspace(_dims(max_ctx=256, num_splits=1))
     many = tt.tt_denoise_attn_workspace(_dims(max_ctx=256, num_splits=4))
     assert many > 3 * small // 2
+
+
+def test_lmhead_validation():
+    f = tt.lib.tt_lmhead_unmask
+    ok_sampler = tt.tt_sampler(0, 0.8, 1.0, 16)
+
+    def call(B=2, S=16, H=256, V=1024, mask=3, sampler=ok_sampler, hidden=16, w=16, ids=16, steps=16):
+        return f(hidden, w, ids, None, steps, None, None, None, B, S, H, V, mask, ctypes.byref(sampler),
+                 16, 1 << 20, None)
+    assert call(B=0) == tt.TT_ERR_INVALID_ARG
+    assert call(S=33) == tt.TT_ERR_UNSUPPORTED
+    assert call(B=200, S=32) == tt.TT_ERR_UNSUPPORTED  # B*S above 4096
+    assert call(H=100) == tt.TT_ERR_UNSUPPORTED        # H % 8
+    assert call(H=32) == tt.TT_ERR_UNSUPPORTED         # H below one 64-wide slice
+    assert call(V=32) == tt.TT_ERR_UNSUPPORTED         # V below one 64-row box
+    assert call(mask=1024) == tt.TT_ERR_INVALID_ARG
+    assert call(sampler=tt.tt_sampler(3, 0.8, 1.0, 16)) == tt.TT_ERR_INVALID_ARG
+    assert call(sampler=tt.tt_sampler(0, 0.8, 0.0, 16)) == tt.TT_ERR_INVALID_ARG
+    assert call(sampler=tt.tt_sampler(0, 0.8, 1.0, 0)) == tt.TT_ERR_INVALID_ARG
+    assert call(hidden=None) == tt.TT_ERR_INVALID_ARG
+    assert call(hidden=24) == tt.TT_ERR_INVALID_ARG and b"aligned" in tt.lib.tt_last_error()
+    assert call(w=None) == tt.TT_ERR_INVALID_ARG
+    assert call(steps=None) == tt.TT_ERR_INVALID_ARG
+    assert tt.tt_lmhead_unmask_workspace(2, 33, 256) == 0
+
+
+def test_qkv_validation():
+    f = tt.lib.tt_qkv_project
+
+    def call(B=2, S=16, H=256, Hq=4, Hkv=1, D=64, y=16, w=16, q=16, k=16, v=16):
+        return f(y, w, q, k, v, B, S, H, Hq, Hkv, D, None)
+    assert call(D=96) == tt.TT_ERR_UNSUPPORTED
+    assert call(Hq=3, Hkv=2) == tt.TT_ERR_INVALID_ARG
+    assert call(B=0) == tt.TT_ERR_INVALID_ARG
+    assert call(H=32) == tt.TT_ERR_UNSUPPORTED
+    assert call(H=100) == tt.TT_ERR_UNSUPPORTED
+    assert call(y=None) == tt.TT_ERR_INVALID_ARG
+    assert call(w=None) == tt.TT_ERR_INVALID_ARG
+    assert call(q=24) == tt.TT_ERR_INVALID_ARG and b"aligned" in tt.lib.tt_last_error()
+    assert call(v=None) == tt.TT_ERR_INVALID_ARG
+
+
+def test_step_kind_and_projection_flags_validated():
+    d = tt.step_desc(_dims(), 2688, 131072, 3, 0.8, 16, 1e-5, 0, 0, 5, 0.0, 20.0)
+    assert tt.tt_denoise_workspace(d) == 0  # logits.kind outside 0, 1, TT_LOGITS_LM_HEAD
+    d = tt.step_desc(_dims(), 2688, 131072, 3, 0.8, 16, 1e-5, 0, 0, 0, 0.0, 20.0)
+    d.qkv_proj = 2
+    assert tt.tt_denoise_workspace(d) == 0
+    d.qkv_proj = 1
+    assert tt.tt_denoise_workspace(d) > 0   # the projection needs no workspace of its own
+    d = tt.step_desc(_dims(D=96), 2688, 131072, 3, 0.8, 16, 1e-5, 0, 0, 0, 0.0, 20.0, qkv_proj=True)
+    assert tt.tt_denoise_workspace(d) == 0
