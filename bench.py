@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.5,
                     help="keep warming up for at least this long so the clock sampler sees load")
-    ap.add_argument("--kernel-only", choices=("attn", "unmask", "adaln", "logits", "step", "lmhead"),
+    ap.add_argument("--kernel-only", choices=("attn", "unmask", "adaln", "logits", "step", "lmhead", "qkv"),
                     default=None,
                     help="profiling aid: run only --reps standalone calls of one entry point on "
                          "the workload (after 3 untimed ones) and print their mean time")
@@ -467,6 +467,12 @@ def kernel_only(wb: Workbench, which: str, reps: int):
         logits = torch.empty((B, S, w.V), dtype=torch.float32, device="cuda")
     tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
     y = torch.empty((B, S, w.H), dtype=torch.int16, device="cuda")
+    if which == "qkv":
+        Wq = wb.w_qkv if wb.w_qkv is not None else wb._dev(synth.make_qkv_weights(w, wb.seed))
+        hq = wb._dev(synth.make_hidden(w, wb.seed))
+        qo = torch.empty((B, S, w.Hq, w.D), dtype=torch.int16, device="cuda")
+        ko = torch.empty((B, S, w.Hkv, w.D), dtype=torch.int16, device="cuda")
+        vo = torch.empty_like(ko)
     if which == "lmhead":
         W = wb.w_vocab if wb.w_vocab is not None else wb._dev(synth.make_lmhead_weights(w, wb.seed))
         h = wb._dev(synth.make_hidden(w, wb.seed))
@@ -487,6 +493,8 @@ def kernel_only(wb: Workbench, which: str, reps: int):
                                  eps=w.ln_eps, row_index=wb.t["n_masked"], table_rows=S + 1)
         elif which == "logits":
             tt.tt_synthetic_logits(spec, logits, B, S, w.V, w.mask_id)
+        elif which == "qkv":
+            tt.tt_qkv_project(hq, Wq, qo, ko, vo, B, S, w.H, w.Hq, w.Hkv, w.D)
         elif which == "lmhead":
             ids.copy_(ids0)
             steps.zero_()

@@ -119,9 +119,19 @@ __global__ void __launch_bounds__(256) lmhead_gather_kernel(LmHeadParams p) {
     }
     const int row = blockIdx.x * kGatherRows + warp;
     if (warp < kGatherRows && row < n && sdest[row] >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.h + (size_t)row * p.H);
-        uint4* dst = reinterpret_cast<uint4*>(p.a_c + (size_t)sdest[row] * p.H);
-        for (int c = lane; c < p.H / 8; c += 32) dst[c] = __ldcg(src + c);
+        // Eight 16-byte loads per lane in flight before any store (2688 bf16 = two rounds).
+        const uint4* __restrict__ src = reinterpret_cast<const uint4*>(p.h + (size_t)row * p.H);
+        uint4* __restrict__ dst = reinterpret_cast<uint4*>(p.a_c + (size_t)sdest[row] * p.H);
+        const int n16 = p.H / 8;
+        for (int c0 = lane; c0 < n16; c0 += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + 32 * u < n16) v[u] = __ldcg(src + c0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+        }
     }
 }
 
