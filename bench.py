@@ -125,7 +125,7 @@ def load_peaks():
 
 
 def workload(args) -> synth.Workload:
-    w = synth.CONFIGS[args.config]
+    w = synth.WORKLOADS[args.config]
     if args.gamma is not None:
         w = w.replace(gamma=args.gamma)
     return w

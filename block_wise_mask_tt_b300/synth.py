@@ -198,8 +198,8 @@ class Workload:
 
 
 # The five workloads of the tiny / single-sequence / batched / long-context / ragged-paged
-# denoise step.  Config 0 names no hidden size; 256 is used for its adaLN.
-CONFIGS = (
+# denoise step.  The tiny one names no hidden size; 256 is used for its adaLN.
+WORKLOADS = (
     Workload("c0_tiny_B1_L256_S16_G4_D64", B=1, L=256, S=16, Hq=4, Hkv=1, D=64, H=256, V=1024,
              softmax_scale=1.0 / 8.0, qkv_fp32_source=True, boost_lo=0.0, boost_hi=12.0),
     Workload("c1_single_B1_L4096_S16_32q2kv_D128", B=1, L=4096, S=16, Hq=32, Hkv=2, D=128,
@@ -212,6 +212,7 @@ CONFIGS = (
              Hkv=2, D=128, H=2688, V=131072, q_prescale=1.0 / math.sqrt(128.0), paged=True,
              logits_kind=LOGITS_BIMODAL),
 )
+TINY, SINGLE, BATCHED, LONG_CONTEXT, RAGGED_PAGED = WORKLOADS
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:

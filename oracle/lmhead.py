@@ -7,7 +7,7 @@ the denoiser predicts all masked positions of the block, i.e. its LM head turns 
 hidden row of each masked position into logits over the vocabulary, and the
 confidence-unmasking step (oracle/unmask.py, oracle/samplers.py) reads those logits.
 
-Readings where the pages are silent (listed in the design doc as well):
+Readings where the pages are silent:
 * the head is a linear map without bias: logit[j] = sum_k h[k] * W[j][k], W stored as
   [V][H] (one row per token id, the layout of a linear layer's weight);
 * the hidden rows are bf16 and so is W; the product is taken exactly (fp64);

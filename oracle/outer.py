@@ -10,7 +10,7 @@ caches, and the loop continues with the next block.  The MLX port's README
 ("Configuration (diffusion)") adds the two stopping knobs: a number of new tokens (a
 multiple of the block size) and an end-of-sequence id.
 
-Readings where the pages are silent (listed in the design doc as well):
+Readings where the pages are silent:
 * the context tower's forward needs trained weights; the keys/values it would append
   for a committed block are stood in for by that block's own keys/values (k_blk,
   v_blk), written at logical positions ctx_len .. ctx_len + S - 1 of the sequence's

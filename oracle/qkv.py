@@ -9,7 +9,7 @@ projections of its hidden states; the block attends over the context tower's cac
 followed by those keys/values).  So at every step Q, K_blk and V_blk are linear
 images of the t-modulated hidden rows.
 
-Readings where the pages are silent (listed in the design doc as well):
+Readings where the pages are silent:
 * one fused projection without bias, W_qkv stored [(Hq + 2 Hkv) D][H]: output column
   c < Hq D is query head c // D, lane c % D; the next Hkv D columns are the keys (kv
   head, lane), the last Hkv D the values - the layout [B][S][heads][D] of q, k_blk,

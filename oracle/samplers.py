@@ -12,7 +12,7 @@ Sources ("Nemotron-Labs-TwoTower" wiki page):
 * the opening summary describes a "mock-AR" two-tower mode that predicts one token per
   step.
 
-Readings where the pages are silent (each is stated in the design doc as well):
+Readings where the pages are silent:
 * temperature tau > 0 divides the logits before the softmax: the confidence of a
   masked position is max_j softmax(l / tau)_j with the mask id removed; the predicted
   token (the argmax, lowest id on ties) does not depend on tau;

@@ -25,7 +25,7 @@ def _check(y_bits, ref, shift):
 
 @pytest.mark.parametrize("B,S,H", [(1, 16, 256), (1, 16, 2688), (4, 32, 2688), (3, 5, 8), (2, 3, 8192)])
 def test_adaln_per_sequence(tt, B, S, H):
-    w = synth.CONFIGS[1].replace(B=B, S=S, H=H)
+    w = synth.SINGLE.replace(B=B, S=S, H=H)
     a = synth.make_adaln_inputs(w, seed=B * 100 + S)
     y = torch.empty((B, S, H), dtype=torch.int16, device="cuda")
     tt.tt_adaln_modulate(dev(a["x"]), dev(a["shift"]), dev(a["scale"]), y, eps=1e-5)
@@ -36,7 +36,7 @@ def test_adaln_per_sequence(tt, B, S, H):
 
 def test_adaln_table_rows(tt):
     B, S, H = 6, 16, 2688
-    w = synth.CONFIGS[1].replace(B=B, S=S, H=H)
+    w = synth.SINGLE.replace(B=B, S=S, H=H)
     a = synth.make_adaln_inputs(w, seed=5)
     rows = np.array([16, 0, 7, 16, 1, 9], np.int32)
     y = torch.empty((B, S, H), dtype=torch.int16, device="cuda")

@@ -152,7 +152,7 @@ def test_lmhead_full_vocabulary(tt, B):
     """H = 2688, V = 131072 as in the single-sequence and batched workloads, all rows
     masked (the first step of a block); the oracle checks sampled sequences."""
     S, H, V, mask = 16, 2688, 131072, 3
-    w = synth.CONFIGS[1].replace(B=B)
+    w = synth.SINGLE.replace(B=B)
     h = synth.make_hidden(w, 3)
     W = synth.make_lmhead_weights(w, 4)
     ids0 = np.full((B, S), mask, np.int32)

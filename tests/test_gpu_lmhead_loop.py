@@ -25,9 +25,9 @@ def tt():
 
 
 CASES = {
-    "tiny_B3_V4096": synth.CONFIGS[0].replace(B=3, V=4096),
-    "single_B2_L512_V16384": synth.CONFIGS[1].replace(B=2, L=512, V=16384),
-    "paged_B4_S32_V8192": synth.CONFIGS[4].replace(B=4, L=700, L_min=64, V=8192, H=512),
+    "tiny_B3_V4096": synth.TINY.replace(B=3, V=4096),
+    "single_B2_L512_V16384": synth.SINGLE.replace(B=2, L=512, V=16384),
+    "paged_B4_S32_V8192": synth.RAGGED_PAGED.replace(B=4, L=700, L_min=64, V=8192, H=512),
 }
 
 

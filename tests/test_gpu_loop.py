@@ -26,11 +26,11 @@ def tt():
 
 
 LOOP_CASES = {
-    "c0": synth.CONFIGS[0],
-    "c1_B2_L512": synth.CONFIGS[1].replace(B=2, L=512),
-    "c4_B3_paged": synth.CONFIGS[4].replace(B=3, L=700, L_min=64, V=16384),
-    "c3_gamma05_B2": synth.CONFIGS[3].replace(B=2, L=256, V=8192, gamma=0.5),
-    "T_lt_S": synth.CONFIGS[0].replace(T=5, gamma=0.97),
+    "c0": synth.TINY,
+    "c1_B2_L512": synth.SINGLE.replace(B=2, L=512),
+    "c4_B3_paged": synth.RAGGED_PAGED.replace(B=3, L=700, L_min=64, V=16384),
+    "c3_gamma05_B2": synth.LONG_CONTEXT.replace(B=2, L=256, V=8192, gamma=0.5),
+    "T_lt_S": synth.TINY.replace(T=5, gamma=0.97),
 }
 
 
@@ -147,7 +147,7 @@ def test_step_by_step_teacher_forced_then_graph_loop(tt, name):
 
 def test_graph_loop_changes_block_index_without_rebuild(tt):
     """Block index / seed enter through the workspace: successive blocks differ as the oracle says."""
-    w = synth.CONFIGS[0]
+    w = synth.TINY
     lp = Loop(tt, w, seed=5, block=0)
     outs = []
     for block in (0, 1, 0):

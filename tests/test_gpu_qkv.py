@@ -85,8 +85,8 @@ def test_qkv_rejects_bad_arguments(tt):
 
 
 STEP_CASES = {
-    "tiny_B2": synth.CONFIGS[0].replace(B=2),
-    "single_B2_L512": synth.CONFIGS[1].replace(B=2, L=512, V=8192, softmax_scale=1.0 / 128 ** 0.5,
+    "tiny_B2": synth.TINY.replace(B=2),
+    "single_B2_L512": synth.SINGLE.replace(B=2, L=512, V=8192, softmax_scale=1.0 / 128 ** 0.5,
                                                q_prescale=1.0),
 }
 

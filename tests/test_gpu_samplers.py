@@ -83,7 +83,7 @@ def test_sampler_unmask_matches_oracle(tt, kind, tau):
 
 @pytest.mark.parametrize("kind,T,tau", [(1, 16, 1.0), (2, 4, 1.0), (2, 5, 0.7), (0, 16, 0.5)])
 def test_block_loop_with_sampler_matches_oracle(tt, kind, T, tau):
-    w = synth.CONFIGS[0].replace(T=T)
+    w = synth.TINY.replace(T=T)
     B, S = w.B, w.S
     inp = synth.make_attention_inputs(w, 4)
     ad = synth.make_adaln_inputs(w, 4)

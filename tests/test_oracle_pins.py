@@ -66,7 +66,7 @@ def test_operating_point_golden():
     import os
     from block_wise_mask_tt_b300 import synth
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "operating_point.json")))
-    for w in synth.CONFIGS[:4]:
+    for w in synth.WORKLOADS[:4]:
         assert w.gamma == g["confidence_threshold"]["value"]
         assert w.S == g["block_size"]["value"]
         assert w.steps_max == g["steps_per_block"]["value"]

@@ -66,7 +66,7 @@ def test_bimodal_boost_ranges():
 
 
 def test_paged_layout_is_a_permutation():
-    w = synth.CONFIGS[4].replace(B=5, L=700, L_min=1, D=8, Hq=4, Hkv=2)
+    w = synth.RAGGED_PAGED.replace(B=5, L=700, L_min=1, D=8, Hq=4, Hkv=2)
     inp = synth.make_attention_inputs(w, 3)
     n = (inp["ctx_len"] + 63) // 64
     used = np.concatenate([inp["page_table"][b, : n[b]] for b in range(w.B)])
@@ -75,7 +75,7 @@ def test_paged_layout_is_a_permutation():
         assert np.all(inp["page_table"][b, n[b]:] == -1)
 
 
-@pytest.mark.parametrize("w", synth.CONFIGS, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", synth.WORKLOADS, ids=lambda w: w.name)
 def test_configs_well_formed(w):
     assert w.Hq % w.Hkv == 0
     assert w.S <= 32 and w.D in (64, 128)

@@ -64,7 +64,7 @@ def _same(a, b, what):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(tt):
-    w = synth.CONFIGS[2].replace(B=12, V=32768)
+    w = synth.BATCHED.replace(B=12, V=32768)
     rng = np.random.default_rng(7)
     # call 1: 12 sequences, some positions already decoded
     ids0 = np.full((w.B, w.S), w.mask_id, np.int64)
