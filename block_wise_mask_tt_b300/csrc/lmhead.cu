@@ -10,7 +10,7 @@
 //  1. lmhead_gather_kernel: every CTA scans ids (B*S <= 4096) for the masked rows and
 //     their compact order; its warps copy their rows' hidden vectors to the compact
 //     matrix a_c, and CTA 0 publishes dest[] and the row count.
-//  2. lmhead_gemm_kernel: one persistent CTA per SM.  A work item is (128-row tile of
+//  2. gemm_kernel<false>: one persistent CTA per SM.  A work item is (128-row tile of
 //     a_c, vocabulary chunk); the chunks split the vocabulary in 64-id units so that
 //     items = row tiles x chunks covers the CTAs once.  Per 256-id vocabulary tile:
 //     warp 0 streams the A tile (128 rows x 64 of H) and four 64-row boxes of W per
@@ -22,9 +22,12 @@
 //     running (max, sum of 2^((x - max) * log2(e) / tau), lowest argmax), with the
 //     mask id and ids past the chunk masked out.  Each item ends with one 16-byte
 //     partial per row.
-//  3. lmhead_finish_kernel: one warp per sequence merges its masked rows' chunk
-//     partials and takes the sampler's commit/remask decision in place (the same
-//     decision code as the unmask kernel).
+//  3. lmhead_finish_kernel: one CTA per sequence; a warp merges each masked row's
+//     chunk partials, then warp 0 takes the sampler's commit/remask decision in place
+//     (the same decision code as the unmask kernel).
+// gemm_kernel<true> is the same GEMM with a bf16 store epilogue: the query/key/value
+// projection of the adaLN output ("Architecture": the block's queries and its own
+// keys/values are the denoiser's projections of its hidden states).
 // Every wait on an mbarrier is bounded; one that runs out sets the error word, the
 // roles drain what they issued, and TMEM is released.
 #include <math_constants.h>
