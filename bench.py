@@ -113,6 +113,8 @@ NCU_TRAFFIC = {
     ("c1_single_B1_L4096_S16_32q2kv_D128", "unmask"): 8.43e6,
     ("c2_batched_B32_L8192_S16_32q2kv_D128", "attn"): 273.23e6 + 0.09e6 + 17.06e6,
     ("c2_batched_B32_L8192_S16_32q2kv_D128", "unmask"): 268.49e6 + 0.11e6,
+    # the LM head's GEMM (profiles/lmhead_gemm_single_B1.md); gather and finish move < 3 MB
+    ("c1_single_B1_L4096_S16_32q2kv_D128", "lmhead"): 707.17e6 + 3.19e6,
 }
 
 
