@@ -105,15 +105,15 @@ def job_throughput(steps_per_rank: int, world: int, elapsed_max_s: float) -> flo
     return world * steps_per_rank / elapsed_max_s
 
 
-# DRAM bytes (read + write) per call of the dominant kernels, from the ncu captures
-# summarised under profiles/ (denoise_step_*.md: cold-cache, per launch).  Missing
-# entries are reported as null.
+# DRAM bytes (read + write) per call of the dominant kernels, from ncu captures of the
+# same kernels (dram__bytes_read.sum + dram__bytes_write.sum, cold cache, per launch).
+# Missing entries, and entries for kernels changed since their capture, are null.
 NCU_TRAFFIC = {
     ("c1_single_B1_L4096_S16_32q2kv_D128", "attn"): 4.41e6 + 4.28e6,
     ("c1_single_B1_L4096_S16_32q2kv_D128", "unmask"): 8.43e6,
     ("c2_batched_B32_L8192_S16_32q2kv_D128", "attn"): 273.23e6 + 0.09e6 + 17.06e6,
     ("c2_batched_B32_L8192_S16_32q2kv_D128", "unmask"): 268.49e6 + 0.11e6,
-    # the LM head's GEMM (profiles/lmhead_gemm_single_B1.md); gather and finish move < 3 MB
+    # the LM head's GEMM; its gather and finish kernels move under 3 MB
     ("c1_single_B1_L4096_S16_32q2kv_D128", "lmhead"): 707.17e6 + 3.19e6,
 }
 
