@@ -831,16 +831,9 @@ tt_status tt_sampler_unmask(const float* logits, int32_t* ids, int32_t* n_masked
                             float* conf, uint8_t* commit, uint8_t* commit_step, int B, int S, int V,
                             int32_t mask_id, const tt_sampler* sampler, void* workspace,
                             size_t workspace_bytes, tt_stream_t stream) {
-    if (sampler == nullptr) return fail(TT_ERR_INVALID_ARG, "sampler is null");
+    TT_TRY(check_sampler(sampler));
     TT_TRY(check_vocab(B, S, V));
     if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
-    if (sampler->kind < TT_SAMPLER_CONFIDENCE || sampler->kind > TT_SAMPLER_PREDICT_NOISE)
-        return fail(TT_ERR_INVALID_ARG, "sampler kind must be a tt_sampler_kind");
-    if (sampler->max_steps < 1 || sampler->max_steps > 255)
-        return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
-    if (sampler->gamma != sampler->gamma) return fail(TT_ERR_INVALID_ARG, "gamma is NaN");
-    if (!(sampler->temperature > 0.f) || !(sampler->temperature < 1e30f))
-        return fail(TT_ERR_INVALID_ARG, "temperature must be positive and finite");
     TT_TRY(need_ptr(logits, "logits"));
     TT_TRY(need_ptr(ids, "ids", false));
     TT_TRY(need_ptr(steps, "steps", false));

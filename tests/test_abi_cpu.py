@@ -205,3 +205,20 @@ def test_step_kind_and_projection_flags_validated():
     assert tt.tt_denoise_workspace(d) > 0   # the projection needs no workspace of its own
     d = tt.step_desc(_dims(D=96), 2688, 131072, 3, 0.8, 16, 1e-5, 0, 0, 0, 0.0, 20.0, qkv_proj=True)
     assert tt.tt_denoise_workspace(d) == 0
+
+
+def test_sampler_unmask_validation():
+    f = tt.lib.tt_sampler_unmask
+    need = tt.tt_confidence_unmask_workspace(2, 16, 1024)
+
+    def call(sampler, mask=3, V=1024):
+        s = None if sampler is None else ctypes.byref(sampler)
+        return f(16, 16, None, 16, None, None, None, 2, 16, V, mask, s, 16, need, None)
+    assert call(None) == tt.TT_ERR_INVALID_ARG
+    assert call(tt.tt_sampler(3, 0.8, 1.0, 16)) == tt.TT_ERR_INVALID_ARG      # unknown kind
+    assert call(tt.tt_sampler(0, 0.8, 1.0, 256)) == tt.TT_ERR_INVALID_ARG     # max_steps
+    assert call(tt.tt_sampler(0, float("nan"), 1.0, 16)) == tt.TT_ERR_INVALID_ARG
+    assert call(tt.tt_sampler(0, 0.8, -1.0, 16)) == tt.TT_ERR_INVALID_ARG     # temperature
+    assert call(tt.tt_sampler(0, 0.8, float("inf"), 16)) == tt.TT_ERR_INVALID_ARG
+    assert call(tt.tt_sampler(1, 0.8, 1.0, 16), mask=1024) == tt.TT_ERR_INVALID_ARG
+    assert call(tt.tt_sampler(2, 0.8, 1.0, 16), V=1022) == tt.TT_ERR_UNSUPPORTED
