@@ -15,18 +15,14 @@ Readings where the pages are silent:
 """
 import numpy as np
 
+from ._bf16 import bf16_to_f64
 from .samplers import sampler_step
-
-
-def bf16_bits_to_f64(bits) -> np.ndarray:
-    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
-    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
 def lm_head_logits(h_bits, W_bits) -> np.ndarray:
     """fp64 logits [n][V] of n hidden rows (bf16 bits [n][H]) through W (bf16 bits [V][H])."""
-    h = bf16_bits_to_f64(h_bits)
-    W = bf16_bits_to_f64(W_bits)
+    h = bf16_to_f64(h_bits)
+    W = bf16_to_f64(W_bits)
     return h @ W.T
 
 

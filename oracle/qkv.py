@@ -19,14 +19,14 @@ Readings where the pages are silent:
 """
 import numpy as np
 
-from .lmhead import bf16_bits_to_f64
+from ._bf16 import bf16_to_f64
 
 
 def qkv_projection(y_bits, W_bits, Hq: int, Hkv: int, D: int):
     """y bf16 bits [B][S][H], W bf16 bits [(Hq + 2 Hkv) D][H] -> fp64 (q [B][S][Hq][D],
     k [B][S][Hkv][D], v [B][S][Hkv][D]), unrounded."""
-    y = bf16_bits_to_f64(y_bits)
-    W = bf16_bits_to_f64(W_bits)
+    y = bf16_to_f64(y_bits)
+    W = bf16_to_f64(W_bits)
     B, S, H = y.shape
     assert W.shape == ((Hq + 2 * Hkv) * D, H)
     out = y.reshape(B * S, H) @ W.T

@@ -162,10 +162,10 @@ def run_unmask(tt, logits: np.ndarray, ids0, steps0, cs0, mask_id, gamma, T):
 
 def _abs_bound(hr, W, rows=16384):
     """max_j sum_k |h_rk W_jk| for every row of hr (bf16 bits), W in blocks of rows."""
-    ha = np.abs(oracle.lmhead.bf16_bits_to_f64(hr))
+    ha = np.abs(bf16_to_f64(hr))
     out = np.zeros(hr.shape[0])
     for v0 in range(0, W.shape[0], rows):
-        Wa = np.abs(oracle.lmhead.bf16_bits_to_f64(W[v0:v0 + rows]))
+        Wa = np.abs(bf16_to_f64(W[v0:v0 + rows]))
         out = np.maximum(out, (ha @ Wa.T).max(axis=1))
     return out
 

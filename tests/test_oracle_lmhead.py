@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
+from gpu_util import bf16_to_f64
 import pins
 from oracle.samplers import sampler_step
 
@@ -19,7 +20,7 @@ def test_lm_head_step(check):
 
 # planted mistakes in copies of the LM head
 def _f64(bits):
-    return oracle.lmhead.bf16_bits_to_f64(bits)
+    return bf16_to_f64(bits)
 
 
 def _logits_mut(h, W, *, transposed=False, half_k=False, bias=False):

@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
+from gpu_util import bf16_to_f64
 import pins
 
 
@@ -12,8 +13,8 @@ def test_qkv(check):
 
 
 def _mut(y, W, Hq, Hkv, D, *, kv_swapped=False, k_from_q=False, transposed_heads=False):
-    yf = oracle.lmhead.bf16_bits_to_f64(y)
-    Wf = oracle.lmhead.bf16_bits_to_f64(W)
+    yf = bf16_to_f64(y)
+    Wf = bf16_to_f64(W)
     B, S, H = yf.shape
     out = yf.reshape(B * S, H) @ Wf.T
     q = out[:, :Hq * D]
