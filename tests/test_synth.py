@@ -80,3 +80,29 @@ def test_configs_well_formed(w):
     assert w.Hq % w.Hkv == 0
     assert w.S <= 32 and w.D in (64, 128)
     assert w.G * w.S <= 512
+
+
+def test_lm_head_weights_follow_the_recipe():
+    """W [V][H] ~ N(0, (lm_logit_std / sqrt(H))^2): unit-RMS hidden rows then give logits
+    of standard deviation lm_logit_std; the draw is seeded and independent of block size."""
+    w = synth.SINGLE.replace(V=4096, H=512)
+    W = synth.make_lmhead_weights(w, 5)
+    assert W.shape == (4096, 512) and W.dtype == np.uint16
+    Wf = synth.bf16_bits_to_f32(W).astype(np.float64)
+    assert abs(Wf.std() - w.lm_logit_std / np.sqrt(w.H)) < 0.01 * w.lm_logit_std / np.sqrt(w.H)
+    assert abs(Wf.mean()) < 3 * Wf.std() / np.sqrt(Wf.size)
+    h = synth.bf16_bits_to_f32(synth.make_hidden(w.replace(B=2), 6)).astype(np.float64).reshape(-1, w.H)
+    logit_std = (h @ Wf.T).std()
+    assert abs(logit_std - w.lm_logit_std) < 0.05 * w.lm_logit_std
+    assert np.array_equal(W, synth.make_lmhead_weights(w, 5, rows=4096))  # same stream, one block
+    assert not np.array_equal(W, synth.make_lmhead_weights(w, 6))
+
+
+def test_qkv_weights_follow_the_recipe():
+    """W_qkv [(Hq + 2 Hkv) D][H] ~ N(0, 1/H): unit-RMS hidden rows give unit-variance q/k/v."""
+    w = synth.TINY
+    W = synth.make_qkv_weights(w, 2)
+    assert W.shape == ((w.Hq + 2 * w.Hkv) * w.D, w.H) and W.dtype == np.uint16
+    Wf = synth.bf16_bits_to_f32(W).astype(np.float64)
+    assert abs(Wf.std() * np.sqrt(w.H) - 1.0) < 0.02
+    assert np.array_equal(W, synth.make_qkv_weights(w, 2))
