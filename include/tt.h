@@ -348,8 +348,8 @@ TT_API tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids,
  * With logits.kind == TT_LOGITS_LM_HEAD the last two are replaced by the fused LM
  * head and sampler step of tt_lmhead_unmask with hidden = y and W = t->w_vocab (no
  * logits buffer is used; H >= 64, V >= 64, B*S <= 4096).
- * The adaLN output does not feed the attention queries here: the projections that
- * would connect them need trained weights.
+ * Without qkv_proj the adaLN output does not feed the attention: q, k_blk and v_blk
+ * are then the caller's fixed tensors (the trained projections are not available).
  * -------------------------------------------------------------------------------- */
 typedef struct {
     tt_attn_dims attn;      /* B, S, heads, D, cache layout, softmax scale */
