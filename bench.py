@@ -11,10 +11,15 @@ and the timed region covers exactly --steps denoise steps (whole blocks, then si
 tt_denoise_step calls for the remainder).  L2 is flushed before every timed block,
 outside the timed events.
 
-Default workload: single sequence, B=1, L=4096 context, S=16, 32q/2kv heads, D=128,
-H=2688, V=131072, gamma=0.8 (--config 1).  --config 0..4 selects the other workloads.
+Headline workload (--config 4): the ragged paged batch, B=64 sequences with context
+lengths uniform on [512, 32768] in shuffled 64-token pages, S=32, 32q/2kv heads,
+D=128, H=2688, V=131072, gamma=0.8 - the largest workload that fits one GPU.  The
+same JSON line carries one object per other realistic workload (--other-configs,
+default 1,2,3: single sequence, batched, long context), each with its own steps/s,
+kernel times, rooflines and end-to-end figure.
 
-    python bench.py [--gpus N --steps K --warmup W] [--config C] [--impl reference]
+    python bench.py [--gpus N --steps K --warmup W] [--config C] [--other-configs 1,2,3]
+                    [--impl reference]
 """
 from __future__ import annotations
 
@@ -44,7 +49,10 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100, help="timed denoise steps")
     ap.add_argument("--warmup", type=int, default=3, help="untimed warm-up denoise steps (>= 3)")
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--other-configs", default="1,2,3",
+                    help="comma-separated workloads measured after the headline one and reported "
+                         "inside the same JSON line ('' for none)")
     ap.add_argument("--impl", choices=("tt", "reference"), default="tt")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gamma", type=float, default=None)
@@ -105,17 +113,43 @@ def job_throughput(steps_per_rank: int, world: int, elapsed_max_s: float) -> flo
     return world * steps_per_rank / elapsed_max_s
 
 
-# DRAM bytes (read + write) per call of the dominant kernels, from ncu captures of the
-# same kernels (dram__bytes_read.sum + dram__bytes_write.sum, cold cache, per launch).
-# Missing entries, and entries for kernels changed since their capture, are null.
-NCU_TRAFFIC = {
-    ("c1_single_B1_L4096_S16_32q2kv_D128", "attn"): 4.41e6 + 4.28e6,
-    ("c1_single_B1_L4096_S16_32q2kv_D128", "unmask"): 8.43e6,
-    ("c2_batched_B32_L8192_S16_32q2kv_D128", "attn"): 273.23e6 + 0.09e6 + 17.06e6,
-    ("c2_batched_B32_L8192_S16_32q2kv_D128", "unmask"): 268.49e6 + 0.11e6,
-    # the LM head's GEMM; its gather and finish kernels move under 3 MB
-    ("c1_single_B1_L4096_S16_32q2kv_D128", "lmhead"): 707.17e6 + 3.19e6,
+# DRAM bytes (read + write) per call, from ncu captures committed as a table in
+# profiles/ncu_traffic.md: | workload | call | DRAM bytes per call | source | capture |.
+# "source" is the sha256 prefix of the kernel sources the capture ran; when the
+# sources have changed since, the figure no longer describes them and reads as null.
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+CALL_SOURCES = {
+    "attn": ("attn.cu",),
+    "unmask": ("unmask.cu", "unmask_common.cuh"),
+    "lmhead": ("lmhead.cu", "unmask_common.cuh"),
 }
+
+
+def sources_sha(call: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in CALL_SOURCES[call]:
+        with open(os.path.join(ROOT, "block_wise_mask_tt_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(workload_name: str, call: str):
+    """(bytes per call or None, note) for one call of a workload."""
+    if not os.path.exists(TRAFFIC_TABLE):
+        return None, "no committed capture"
+    for line in open(TRAFFIC_TABLE):
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) < 4 or cells[0] != workload_name or cells[1] != call:
+            continue
+        try:
+            nbytes = float(cells[2].replace(",", "").replace(" ", ""))
+        except ValueError:
+            return None, "unparsed capture"
+        if cells[3] != sources_sha(call):
+            return None, f"kernel changed since the capture (capture {cells[3]}, now {sources_sha(call)})"
+        return nbytes, f"ncu capture of sources {cells[3]}, {TRAFFIC_TABLE[len(ROOT) + 1:]}"
+    return None, "no committed capture for this workload"
 
 
 def load_peaks():
@@ -295,8 +329,11 @@ def plan_blocks(wb: Workbench, first_block: int, need_steps: int):
     return plan
 
 
-def run_timed(wb: Workbench, plan, flush, with_events=True):
-    """Runs the plan; returns (elapsed seconds summed over blocks, kernel launches)."""
+def run_timed(wb: Workbench, plan, flush, hist=None):
+    """Runs the plan; returns (elapsed seconds summed over blocks, kernel launches).
+
+    hist (optional, int [S][T]): after each whole block, outside its events, adds one
+    count per committed position at its commit step (position x step histogram)."""
     torch = wb.torch
     elapsed = 0.0
     launches = 0
@@ -317,6 +354,13 @@ def run_timed(wb: Workbench, plan, flush, with_events=True):
         e.record()
         e.synchronize()
         elapsed += s.elapsed_time(e) / 1e3
+        if hist is not None and take == n:
+            cs = wb.t["commit_step"].cpu().numpy().astype(np.int64)
+            S, T = hist.shape
+            for p_ in range(S):
+                k = cs[:, p_]
+                k = k[(k >= 1) & (k <= T)]
+                np.add.at(hist[p_], k - 1, 1)
     return elapsed, launches
 
 
@@ -666,23 +710,23 @@ def oracle_block_time(w: synth.Workload, seed: int, block: int, max_steps=None, 
     return n, dt, B
 
 
-def cpu_baseline(w: synth.Workload, seed: int):
-    budget = 20.0
-    steps = 0
-    secs = 0.0
-    block = 0
+def cpu_baseline(w: synth.Workload, seed: int, budget: float = 20.0):
+    """The oracle on the host cores, on a bounded sample: one sequence of the batch,
+    decoded step by step (whole blocks while they fit), stopping once about half the
+    budget is spent; steps/s scaled to the full batch."""
+    steps, secs, block = 0, 0.0, 0
     b_sample = 1 if w.B > 1 else None
-    while secs < budget and block < 64:
-        n, dt, B = oracle_block_time(w, seed, block, b_sample=b_sample)
+    B = 1
+    while secs < budget / 2 and block < 64:
+        n, dt, B = oracle_block_time(w, seed, block, b_sample=b_sample,
+                                     max_steps=None if w.B == 1 and w.L <= 8192 else 2)
         steps += n
         secs += dt
         block += 1
-        if secs > budget / 2 and block >= 1:
-            break
-    frac = (B / w.B)
+    frac = B / w.B
     # a denoise step of the full batch costs ~1/frac of the sampled one on the CPU
     value = steps / secs * frac
-    sample = (f"{block} block(s) of {B} of {w.B} sequence(s), {steps} denoise steps, "
+    sample = (f"{steps} denoise steps over {block} block(s) of {B} of {w.B} sequence(s), "
               f"{secs:.1f} s; steps/s scaled by {frac:g} to the full batch")
     return {"value": value, "unit": "denoise steps/s", "cores": cores_used(), "kind": "oracle",
             "sample": sample}
@@ -721,6 +765,127 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ main
+def kernel_rooflines(wb: Workbench, ktimes: dict):
+    """Per-kernel figures of the standalone attention and unmask calls, and one roofline
+    object per call (algorithmic work / mean duration against the measured peak)."""
+    peaks, peak_kind = load_peaks()
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    w = wb.w
+    attn_gbs = wb.attn_bytes / ktimes["attn"] / 1e9
+    attn_tfs = wb.attn_flops / ktimes["attn"] / 1e12
+    attn_bound = "hbm" if wb.attn_bytes / hbm / 1e9 >= wb.attn_flops / tc / 1e12 else "tensor"
+    attn_roof = max(wb.attn_bytes / (hbm * 1e9), wb.attn_flops / (tc * 1e12))
+    um_gbs = wb.unmask_bytes_full / ktimes["unmask"] / 1e9
+    kernels = {
+        "tt_denoise_attn": {"us": ktimes["attn"] * 1e6, "GB_s": attn_gbs, "TFLOP_s": attn_tfs,
+                            "bound": attn_bound, "roofline_us": attn_roof * 1e6,
+                            "frac": attn_roof / ktimes["attn"], "algorithmic_bytes": wb.attn_bytes,
+                            "flops": wb.attn_flops},
+        "tt_confidence_unmask": {"us": ktimes["unmask"] * 1e6, "GB_s": um_gbs,
+                                 "roofline_us": wb.unmask_bytes_full / (hbm * 1e9) * 1e6,
+                                 "frac": um_gbs / hbm, "algorithmic_bytes": wb.unmask_bytes_full},
+    }
+    if attn_bound == "hbm":
+        ra = {"kernel": "tt_denoise_attn (split + combine)", "bound": "hbm", "achieved": attn_gbs,
+              "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm}
+    else:
+        ra = {"kernel": "tt_denoise_attn (split + combine)", "bound": "tensor", "achieved": attn_tfs,
+              "peak": tc, "unit": "TFLOP/s", "frac": attn_tfs / tc}
+    ru = {"kernel": "tt_confidence_unmask (first step, all rows masked)", "bound": "hbm",
+          "achieved": um_gbs, "peak": hbm, "unit": "GB/s", "frac": um_gbs / hbm}
+    for r, call in ((ra, "attn"), (ru, "unmask")):
+        r["traffic"], r["traffic_note"] = ncu_traffic(w.name, call)
+        r["traffic_unit"] = "DRAM bytes per call"
+        r["algorithmic_bytes"] = wb.attn_bytes if call == "attn" else wb.unmask_bytes_full
+        r["peak_source"] = peak_kind
+    return kernels, {"tt_denoise_attn": ra, "tt_confidence_unmask": ru}
+
+
+def l2_note(wb: Workbench) -> str:
+    kv = wb.kv_bytes
+    lg = 0 if wb.t["logits"] is None else wb.w.B * wb.w.S * wb.w.V * 4
+    warm = kv + lg < 126e6
+    return ("L2 flushed (512 MiB write) before every timed block, outside the events; within a "
+            f"block the context K/V ({kv / 1e6:.1f} MB) and logits ({lg / 1e6:.1f} MB) "
+            + ("fit in the 126 MB L2, so steps 2..n of a block find them L2-resident"
+               if warm else "exceed the 126 MB L2, so every step streams them from HBM"))
+
+
+def measure_workload(args, tt, torch, w, seed, flush, world, dist, smi_id, legs: bool):
+    """Steps/s of one workload (timed whole blocks), its standalone kernel times and
+    rooflines, and the end-to-end figure through host buffers."""
+    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
+                   args.qkv_proj)
+    warm_plan = plan_blocks(wb, 100_000, max(args.warmup, 3))
+    plan = plan_blocks(wb, 0, args.steps)
+    total_steps = sum(t for _, _, t in plan)
+    hist = np.zeros((w.S, w.steps_max), np.int64)
+    with ClockSampler(smi_id) as clk:
+        t_warm = time.time()
+        run_timed(wb, warm_plan, flush)
+        while time.time() - t_warm < args.min_warmup_s:
+            run_timed(wb, warm_plan, flush)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        elapsed, launches = run_timed(wb, plan, flush, hist)
+    torch.cuda.synchronize()
+    if world > 1:
+        elapsed = max_over_ranks(elapsed, dist, "cuda")
+        dist.barrier()
+    status = tt.tt_device_status(True)
+    if status != 0:
+        raise RuntimeError(f"device-side error {status} during the timed region ({w.name})")
+    ktimes = kernel_times(wb, flush, args.kernel_reps)
+    kernels, roofs = kernel_rooflines(wb, ktimes)
+    lm = qkv = None
+    if legs:
+        lm = None if args.no_lm_head_leg and not args.lm_head else run_lmhead(wb, flush)
+        if lm is not None:
+            kernels["tt_lmhead_unmask"] = {k: lm[k] for k in ("us", "TFLOP_s", "GB_s", "bound", "roofline_us",
+                                                               "frac", "algorithmic_bytes", "flops")}
+        qkv = None if args.no_qkv_leg and not args.qkv_proj else run_qkv(wb, flush)
+        if qkv is not None:
+            kernels["tt_qkv_project"] = {k: qkv[k] for k in ("us", "bound", "roofline_us", "frac",
+                                                            "algorithmic_bytes", "flops")}
+    if args.lm_head and lm is not None and lm["us"] * 1e-6 > ktimes["attn"]:
+        roof = {"kernel": "tt_lmhead_unmask (gather + GEMM + decision, first step)", "bound": lm["bound"],
+                "achieved": lm["achieved"], "peak": lm["peak"], "unit": lm["unit"], "frac": lm["frac"],
+                "peak_source": lm["peak_source"]}
+        roof["traffic"], roof["traffic_note"] = ncu_traffic(w.name, "lmhead")
+        roof["traffic_unit"] = "DRAM bytes per call"
+    else:
+        dominant = "tt_denoise_attn" if ktimes["attn"] >= ktimes["unmask"] else "tt_confidence_unmask"
+        roof = dict(roofs[dominant])
+    e2e = None
+    if not args.no_e2e:
+        e_el, h2d, d2h = run_e2e(wb, plan, torch, tt)
+        if world > 1:
+            e_el = max_over_ranks(e_el, dist, "cuda")
+        e2e = {"value": job_throughput(total_steps, world, e_el), "unit": "denoise steps/s",
+               "h2d_bytes_per_step": int(h2d * len(plan) / total_steps),
+               "d2h_bytes_per_step": int(d2h * len(plan) / total_steps)}
+    whole = [(bi, n, t) for bi, n, t in plan if t == n]
+    res = {
+        "workload": w.name, "value": job_throughput(total_steps, world, elapsed),
+        "unit": "denoise steps/s", "steps": total_steps,
+        "warmup": sum(t for _, _, t in warm_plan), "ms_per_step": 1e3 * elapsed / total_steps,
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "L_min": w.L_min, "S": w.S, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "D": w.D, "H": w.H, "V": w.V, "gamma": w.gamma, "paged": w.paged,
+                   "blocks_timed": len(plan), "whole_blocks": len(whole), "l2": l2_note(wb)},
+        "tokens_per_step": (w.B * w.S * len(whole) / max(1, sum(n for _, n, _ in whole))) if whole else None,
+        "commit_histogram": {"rows": "block position", "cols": "commit step (1-based)",
+                             "counts": hist.tolist()},
+        "roofline": roof,
+        "rooflines": roofs,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    return res, wb, lm, qkv
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -736,9 +901,9 @@ def main():
 
     w = workload(args)
     seed = replica_seed(args.seed, rank)
-    wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
-                   args.qkv_proj)
     if args.kernel_only:
+        wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
+                       args.qkv_proj)
         kernel_only(wb, args.kernel_only, args.reps)
         return
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
@@ -746,92 +911,33 @@ def main():
     def flush():
         flush_buf.zero_()
 
-    warm = max(args.warmup, 3)
-    warm_plan = plan_blocks(wb, 100_000, warm)
-    plan = plan_blocks(wb, 0, args.steps)
-    total_steps = sum(t for _, _, t in plan)
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:
         smi_id = str(local)
 
-    with ClockSampler(smi_id) as clk:
-        t_warm = time.time()
-        run_timed(wb, warm_plan, flush)
-        while time.time() - t_warm < args.min_warmup_s:
-            run_timed(wb, warm_plan, flush)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        elapsed, launches = run_timed(wb, plan, flush)
-    torch.cuda.synchronize()
-    if world > 1:
-        elapsed = max_over_ranks(elapsed, dist, "cuda")
-        dist.barrier()
-    status = tt.tt_device_status(True)
-    if status != 0:
-        raise RuntimeError(f"device-side error {status} during the timed region")
-
-    value = job_throughput(total_steps, world, elapsed)
-    peaks, peak_kind = load_peaks()
-    ktimes = kernel_times(wb, flush, args.kernel_reps)
-    hbm = peaks["hbm_gbs"]
-    tc = peaks["bf16_tflops"]
-    attn_gbs = wb.attn_bytes / ktimes["attn"] / 1e9
-    attn_tfs = wb.attn_flops / ktimes["attn"] / 1e12
-    attn_bound = "hbm" if wb.attn_bytes / hbm / 1e9 >= wb.attn_flops / tc / 1e12 else "tensor"
-    attn_roof = max(wb.attn_bytes / (hbm * 1e9), wb.attn_flops / (tc * 1e12))
-    um_gbs = wb.unmask_bytes_full / ktimes["unmask"] / 1e9
-    kernels = {
-        "tt_denoise_attn": {"us": ktimes["attn"] * 1e6, "GB_s": attn_gbs, "TFLOP_s": attn_tfs,
-                            "bound": attn_bound, "roofline_us": attn_roof * 1e6,
-                            "frac": attn_roof / ktimes["attn"], "algorithmic_bytes": wb.attn_bytes,
-                            "flops": wb.attn_flops},
-        "tt_confidence_unmask": {"us": ktimes["unmask"] * 1e6, "GB_s": um_gbs,
-                                 "roofline_us": wb.unmask_bytes_full / (hbm * 1e9) * 1e6,
-                                 "frac": um_gbs / hbm, "algorithmic_bytes": wb.unmask_bytes_full},
-    }
-    lm = None if args.no_lm_head_leg and not args.lm_head else run_lmhead(wb, flush)
-    if lm is not None:
-        kernels["tt_lmhead_unmask"] = {k: lm[k] for k in ("us", "TFLOP_s", "GB_s", "bound", "roofline_us",
-                                                           "frac", "algorithmic_bytes", "flops")}
-    qkv = None if args.no_qkv_leg and not args.qkv_proj else run_qkv(wb, flush)
-    if qkv is not None:
-        kernels["tt_qkv_project"] = {k: qkv[k] for k in ("us", "bound", "roofline_us", "frac",
-                                                        "algorithmic_bytes", "flops")}
-    if args.lm_head:
-        dominant = "attn" if ktimes["attn"] >= lm["us"] * 1e-6 else "lmhead"
-    else:
-        dominant = "attn" if ktimes["attn"] >= ktimes["unmask"] else "unmask"
-    if dominant == "lmhead":
-        roof = {"kernel": "tt_lmhead_unmask (gather + GEMM + decision, first step)", "bound": lm["bound"],
-                "achieved": lm["achieved"], "peak": lm["peak"], "unit": lm["unit"], "frac": lm["frac"]}
-    elif dominant == "attn":
-        if attn_bound == "hbm":
-            roof = {"kernel": "tt_denoise_attn (split + merge)", "bound": "hbm", "achieved": attn_gbs,
-                    "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm}
-        else:
-            roof = {"kernel": "tt_denoise_attn (split + merge)", "bound": "tensor",
-                    "achieved": attn_tfs, "peak": tc, "unit": "TFLOP/s", "frac": attn_tfs / tc}
-    else:
-        roof = {"kernel": "tt_confidence_unmask (first step, all rows masked)", "bound": "hbm",
-                "achieved": um_gbs, "peak": hbm, "unit": "GB/s", "frac": um_gbs / hbm}
-    roof["traffic"] = NCU_TRAFFIC.get((w.name, dominant))
-    roof["traffic_unit"] = "bytes per call"
-    roof["peak_source"] = peak_kind
-
-    e2e = None
-    if not args.no_e2e:
-        e_el, h2d, d2h = run_e2e(wb, plan, torch, tt)
-        if world > 1:
-            e_el = max_over_ranks(e_el, dist, "cuda")
-        e2e = {"value": job_throughput(total_steps, world, e_el), "unit": "denoise steps/s",
-               "h2d_bytes_per_step": int(h2d * len(plan) / total_steps),
-               "d2h_bytes_per_step": int(d2h * len(plan) / total_steps)}
-
+    head, wb, lm, qkv = measure_workload(args, tt, torch, w, seed, flush, world, dist, smi_id, legs=True)
     gen_line = None
-    if args.generate > 0 and not w.paged:
-        gen_line = run_generate(wb, args.generate, flush)
+    others = {}
+    other_ids = [int(c) for c in args.other_configs.split(",") if c.strip() != ""]
+    other_ids = [c for c in other_ids if c != args.config]
+    del wb
+    for c in other_ids:
+        torch.cuda.empty_cache()
+        wc = synth.WORKLOADS[c]
+        if args.gamma is not None:
+            wc = wc.replace(gamma=args.gamma)
+        res, wbc, _, _ = measure_workload(args, tt, torch, wc, seed, flush, world, dist, smi_id, legs=False)
+        if gen_line is None and args.generate > 0 and not wc.paged:
+            gen_line = run_generate(wbc, args.generate, flush)
+            gen_line["workload"] = wc.name
+        others[wc.name] = res
+        del wbc
+    if gen_line is None and args.generate > 0 and not w.paged:
+        wbh = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
+                        args.qkv_proj)
+        gen_line = run_generate(wbh, args.generate, flush)
+        gen_line["workload"] = w.name
 
     if rank != 0:
         if world > 1:
@@ -841,30 +947,30 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(w, seed)
-    blocks_full = sum(1 for _, n, t in plan if t == n)
+    cfg = dict(head["config"])
+    cfg.update({"bench_step": "one denoise step of the whole batch",
+                "logits": ("fused LM head over the adaLN output (synthetic W [V][H], resident)"
+                           if args.lm_head else "hash stand-in"),
+                "qkv": ("projected from the adaLN output every step (synthetic W_qkv, resident)"
+                        if args.qkv_proj else "fixed synthetic tensors"),
+                "sampler": args.sampler, "temperature": args.temperature,
+                "parallelism": f"replicas{world}"})
     line = {
-        "metric": METRIC, "value": value, "unit": "denoise steps/s", "n_gpus": world,
-        "steps": total_steps, "warmup": sum(t for _, _, t in warm_plan),
-        "ms_per_step": 1e3 * elapsed / total_steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "D": w.D, "H": w.H, "V": w.V, "gamma": w.gamma, "paged": w.paged,
-                   "bench_step": "one denoise step of the whole batch",
-                   "logits": ("fused LM head over the adaLN output (synthetic W [V][H], resident)"
-                              if args.lm_head else "hash stand-in"),
-                   "qkv": ("projected from the adaLN output every step (synthetic W_qkv, resident)"
-                           if args.qkv_proj else "fixed synthetic tensors"),
-                   "sampler": args.sampler, "temperature": args.temperature,
-                   "blocks_timed": len(plan), "whole_blocks": blocks_full,
-                   "tokens_per_step": w.B * w.S * blocks_full / max(1, sum(t for _, n, t in plan if t == n)),
-                   "l2": "flushed (512 MiB write) before every timed block, outside the events",
-                   "parallelism": f"replicas{world}"},
-        "roofline": roof,
-        "kernels": kernels,
+        "metric": METRIC, "value": head["value"], "unit": "denoise steps/s", "n_gpus": world,
+        "steps": head["steps"], "warmup": head["warmup"], "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": cfg,
+        "tokens_per_step": head["tokens_per_step"],
+        "roofline": head["roofline"],
+        "rooflines": head["rooflines"],
+        "kernels": head["kernels"],
         "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "commit_histogram": head["commit_histogram"],
+        "configs": others,
         "generate": gen_line,
         "lm_head": lm,
         "qkv_proj": qkv,

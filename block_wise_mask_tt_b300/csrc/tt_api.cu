@@ -1076,4 +1076,13 @@ tt_status tt_qkv_project(const void* y, const void* w_qkv, void* q, void* k_blk,
     return enqueue_qkv(y, w_qkv, q, k_blk, v_blk, B, S, H, Hq, Hkv, D, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tt_status tt_selftest_wait_timeout(uint32_t limit_us, tt_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000u)
+        return fail(TT_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+    int* err = nullptr;
+    TT_TRY(device_err_word(&err));
+    TT_CUDA(tti::launch_wait_timeout(err, 1000ull * limit_us, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+    return TT_OK;
+}
+
 }  // extern "C"

@@ -243,4 +243,11 @@ struct LoopCondParams {
 };
 cudaError_t launch_loop_cond(const LoopCondParams& p, cudaStream_t stream);
 
+// ------------------------------------------------------------------------- self-test
+// One CTA waits on an mbarrier nothing arrives on, for limit_ns, through the bounded
+// wait of every kernel; when the wait runs out it sets TT_ERR_TIMEOUT in *err and
+// writes 1 to *waited_out (nullable), else 0.
+cudaError_t launch_wait_timeout(int* err, unsigned long long limit_ns, int* waited_out,
+                                cudaStream_t stream);
+
 }  // namespace tti

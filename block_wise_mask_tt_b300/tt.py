@@ -103,6 +103,7 @@ _SIGS = {
     "tt_lmhead_unmask": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_int32,
                               ctypes.POINTER(tt_sampler), _P, ctypes.c_size_t, _P]),
     "tt_qkv_project": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "tt_selftest_wait_timeout": (_I, [ctypes.c_uint32, _P]),
     "tt_denoise_workspace": (ctypes.c_size_t, [ctypes.POINTER(tt_step_desc)]),
     "tt_append_block": (_I, [ctypes.POINTER(tt_attn_dims), _P, _P, _P, _P, _P, _P, _P,
                              ctypes.POINTER(tt_stop_spec), _P, _P, _P, _I, _I, _P]),
@@ -278,6 +279,12 @@ def tt_confidence_unmask_noalloc(logits, ids, steps, B, S, V, mask_id, gamma, ma
         _ptr(conf, "conf", _F32, B * S), _ptr(commit, "commit", _U8, B * S),
         _ptr(commit_step, "commit_step", _U8, B * S), B, S, V, int(mask_id), float(gamma),
         int(max_steps), _stream(stream)))
+
+
+def tt_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launches a wait that is meant to run out after limit_us microseconds (the
+    library's failure path); tt_device_status() then reports TT_ERR_TIMEOUT."""
+    _check(lib.tt_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def step_desc(attn: tt_attn_dims, H, V, mask_id, gamma, max_steps, ln_eps, seed, block_index,

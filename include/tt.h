@@ -335,6 +335,23 @@ TT_API tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids,
                                               int max_steps, tt_stream_t stream);
 
 /* --------------------------------------------------------------------------------
+ * Self-test of the device-side failure path (no counterpart on the pages: it belongs
+ * to this library's error handling, not to the method)
+ *
+ * Every wait inside the library's kernels (on a TMA copy, a tensor-core operation or
+ * another warp) is bounded; a wait that runs out sets TT_ERR_TIMEOUT in the device
+ * error word, the kernel drains what it issued and returns, and the context stays
+ * usable.  This call exercises exactly that path on purpose: one CTA initialises an
+ * mbarrier in shared memory that nothing ever arrives on, waits on it for limit_us
+ * microseconds (1 .. 1 000 000) through the same bounded-wait helper, and reports the
+ * timeout.  It touches no caller memory, faults nothing and always ends.
+ * Afterwards tt_device_status() returns TT_ERR_TIMEOUT (and reset clears it).
+ * Errors: TT_ERR_INVALID_ARG for limit_us outside the range; TT_ERR_CUDA if the launch
+ * fails.
+ * -------------------------------------------------------------------------------- */
+TT_API tt_status tt_selftest_wait_timeout(uint32_t limit_us, tt_stream_t stream);
+
+/* --------------------------------------------------------------------------------
  * Whole denoise step and whole block (a1..a5 chained on the device)
  *
  * "Nemotron-Labs-TwoTower" wiki, "Block-wise generation": a block starts fully

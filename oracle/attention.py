@@ -84,11 +84,15 @@ def denoise_attention_rows(inp: dict, softmax_scale: float, rows):
         kc, vc = context_kv(inp, b)
         kb = bf16_to_f64(inp["k_blk"][b])
         vb = bf16_to_f64(inp["v_blk"][b])
+        by_g = {}
         for i, s, h in items:
-            g = h // G
+            by_g.setdefault(h // G, []).append((i, s, h))
+        for g, rows_g in by_g.items():
+            # the concatenated keys/values of kv head g, built once for all its rows
             keys = np.concatenate([kc[:, g, :], kb[:, g, :]], axis=0)
             vals = np.concatenate([vc[:, g, :], vb[:, g, :]], axis=0)
-            qs = bf16_to_f64(inp["q"][b, s, h])[None, :]
-            o, l = _head_attention(qs, keys, vals, softmax_scale)
-            O[i], lse[i] = o[0], l[0]
+            for i, s, h in rows_g:
+                qs = bf16_to_f64(inp["q"][b, s, h])[None, :]
+                o, l = _head_attention(qs, keys, vals, softmax_scale)
+                O[i], lse[i] = o[0], l[0]
     return O, lse

@@ -31,3 +31,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """One line per workload: sequence decisions left out of the bit-exact comparison
+    because a confidence lay within 1e-5 of gamma (or the floor compared confidences
+    that close); they were checked for validity instead."""
+    try:
+        from gpu_util import EXCLUDED
+    except Exception:
+        return
+    if not EXCLUDED:
+        return
+    terminalreporter.write_sep("-", "gamma-band exclusions (validity-checked, not bit-exact)")
+    for key in sorted(EXCLUDED):
+        n, total = EXCLUDED[key]
+        terminalreporter.write_line(f"{key}: {n} of {total} sequence decisions excluded")

@@ -37,6 +37,17 @@ CONF_REL = 1e-5
 GAMMA_BAND = 1e-5
 
 
+# gamma-band exclusions per workload, reported at the end of the run (conftest.py):
+# key -> [sequences excluded, sequence decisions compared]
+EXCLUDED = {}
+
+
+def record_excluded(key: str, excluded: int, decisions: int) -> None:
+    e = EXCLUDED.setdefault(key, [0, 0])
+    e[0] += int(excluded)
+    e[1] += int(decisions)
+
+
 def dev(a: np.ndarray) -> torch.Tensor:
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint16:
@@ -111,8 +122,59 @@ def ambiguous(r: dict, ids0_b: np.ndarray, mask_id: int, gamma: float) -> bool:
     return False
 
 
-def compare_unmask(gpu: dict, ora: list, ids0, steps0, mask_id, gamma, what="") -> int:
-    """Asserts parity of one unmask call for a batch; returns the number of excluded sequences."""
+def check_decision_validity(ids_g, com, ids0_b, tok, conf, mask_id, kind, gamma, k_min, band,
+                            what=""):
+    """The sampler decision of one sequence is one that the rule could have taken.
+
+    ``conf`` holds the oracle's confidences (0 at decoded positions) and ``band`` the
+    largest difference allowed between the kernel's confidence and the oracle's
+    (scalar or per position), so the kernel's value of position i lies in
+    [conf_i - band_i, conf_i + band_i].  The commit set C must then satisfy:
+    * confidence rule (kind 0): either C is the threshold set - every position whose
+      confidence is certainly >= gamma is in C and none that is certainly < gamma -
+      and |C| >= k_min; or fewer than k_min are certainly >= gamma and C is a
+      possible top-k_min (the floor);
+    * predict-and-noise (kind 2): C is a possible top-k_min;
+    * mock-AR (kind 1): C is the leftmost masked position;
+    where a "possible top-k" has k elements and no position left out certainly
+    beats one taken.  Committed tokens are the oracle's argmax, the other masked
+    positions keep the mask id, decoded positions are unchanged."""
+    masked = ids0_b == mask_id
+    com = np.asarray(com).astype(bool)
+    band = np.broadcast_to(np.asarray(band, dtype=np.float64), conf.shape)
+    assert np.all(~com | masked), f"{what}: commit at a decoded position"
+    assert np.array_equal(ids_g[~masked], ids0_b[~masked]), f"{what}: decoded position changed"
+    assert np.array_equal(ids_g[com], tok[com]), f"{what}: committed token is not the oracle's argmax"
+    assert np.all(ids_g[masked & ~com] == mask_id), f"{what}: uncommitted position not remasked"
+    n = int(com.sum())
+    lo, hi = conf - band, conf + band
+
+    def possible_topk(k):
+        if n != k:
+            return False
+        taken, left = masked & com, masked & ~com
+        return not (taken.any() and left.any() and lo[left].max() > hi[taken].min())
+
+    if kind == 1:
+        pos = np.flatnonzero(masked)
+        ok = pos.size == 0 or (n == 1 and com[pos[0]])
+    elif kind == 2:
+        ok = possible_topk(k_min)
+    else:
+        sure = masked & (lo >= gamma)
+        maybe = masked & (hi >= gamma)
+        threshold_set = bool(np.all(com[sure]) and np.all(~com | maybe) and n >= k_min)
+        ok = threshold_set or (int(sure.sum()) < k_min and possible_topk(k_min))
+    assert ok, (f"{what}: commit set {np.flatnonzero(com).tolist()} is not one the rule allows "
+                f"(k_min {k_min}, confidences {np.round(conf[masked], 7).tolist()})")
+
+
+def compare_unmask(gpu: dict, ora: list, ids0, steps0, mask_id, gamma, what="", kind=0) -> int:
+    """Asserts parity of one unmask call for a batch; returns the number of excluded sequences.
+
+    Every sequence is checked for validity (check_decision_validity, with the
+    confidence tolerance as the band); sequences that are not ambiguous must then
+    match the oracle bit for bit."""
     excluded = 0
     B = ids0.shape[0]
     for b in range(B):
@@ -124,40 +186,77 @@ def compare_unmask(gpu: dict, ora: list, ids0, steps0, mask_id, gamma, what="") 
         if masked.any():
             rel = np.abs(cg[masked] - co[masked]) / np.maximum(co[masked], 1e-300)
             assert rel.max() <= CONF_REL, f"{what} b={b}: conf rel err {rel.max()}"
+        assert gpu["steps"][b] == r["steps"], f"{what} b={b}: steps differ"
+        check_decision_validity(gpu["ids"][b], gpu["commit"][b], ids0[b], r["tok"], co, mask_id, kind,
+                                gamma, r["k_min"], CONF_REL * co, what=f"{what} b={b}")
+        com = gpu["commit"][b].astype(bool)
+        assert gpu["n_masked"][b] == int(masked.sum()) - int(com.sum()), f"{what} b={b}: n_masked"
+        # commit_step: the new step count where the kernel committed; elsewhere the value
+        # from before the step (the oracle's, with its own commits of this step undone:
+        # positions masked before the step hold 0)
+        before = np.where(r["commit"].astype(bool), 0, r["commit_step"])
+        exp_cs = np.where(com, r["steps"], before).astype(np.uint8)
+        assert np.array_equal(gpu["commit_step"][b], exp_cs), f"{what} b={b}: commit_step"
         if ambiguous(r, ids0[b], mask_id, gamma):
             excluded += 1
-            # validity only: committed tokens are the oracle's argmax, decoded positions
-            # unchanged, one step taken, counts consistent
-            com = gpu["commit"][b].astype(bool)
-            assert np.all(~com | masked)
-            assert np.array_equal(gpu["ids"][b][com], r["tok"][com])
-            assert np.array_equal(gpu["ids"][b][~masked], ids0[b][~masked])
-            assert np.all(gpu["ids"][b][masked & ~com] == mask_id)
-            assert gpu["steps"][b] == r["steps"]
-            assert com.sum() >= r["k_min"]
             continue
         assert np.array_equal(gpu["ids"][b], r["ids"]), f"{what} b={b}: ids differ"
         assert np.array_equal(gpu["commit"][b], r["commit"]), f"{what} b={b}: commit differs"
-        assert gpu["steps"][b] == r["steps"], f"{what} b={b}: steps differ"
         assert gpu["n_masked"][b] == r["n_masked"], f"{what} b={b}: n_masked differs"
         assert np.array_equal(gpu["commit_step"][b], r["commit_step"]), f"{what} b={b}: commit_step"
     return excluded
 
 
+GUARD = 4096  # canary elements on each side of a guarded output buffer
+
+
+def guarded(n, dtype, fill):
+    """A flat device buffer with GUARD canary elements of `fill` on both sides;
+    returns (whole buffer, the n-element view handed to the kernel)."""
+    full = torch.full((n + 2 * GUARD,), fill, dtype=dtype, device="cuda")
+    return full, full[GUARD:GUARD + n]
+
+
+def guarded_copy(a: np.ndarray, canary):
+    """The host array a on the device inside canaries: (whole buffer, view of a's shape)."""
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    full, view = guarded(t.numel(), t.dtype, canary)
+    view.copy_(t.reshape(-1).cuda())
+    return full, view.view(t.shape)
+
+
+def check_guards(full, fill, what=""):
+    """The canaries around a guarded buffer are untouched (NaN canaries stay NaN)."""
+    g = torch.cat([full[:GUARD], full[-GUARD:]])
+    if isinstance(fill, float) and math.isnan(fill):
+        ok = bool(torch.isnan(g).all())
+    else:
+        ok = bool((g == fill).all())
+    assert ok, f"{what}: the kernel wrote outside its buffer"
+
+
 def run_unmask(tt, logits: np.ndarray, ids0, steps0, cs0, mask_id, gamma, T):
+    """One tt_confidence_unmask call on host inputs; every buffer it writes sits between
+    canaries that must come back untouched."""
     B, S, V = logits.shape
     d_logits = dev(logits.astype(np.float32))
-    ids = dev(ids0.astype(np.int32))
-    steps = dev(steps0.astype(np.int32))
-    cs = dev(cs0.astype(np.uint8))
-    n_masked = torch.zeros(B, dtype=torch.int32, device="cuda")
-    conf = torch.full((B, S), -1.0, dtype=torch.float32, device="cuda")
-    commit = torch.full((B, S), 7, dtype=torch.uint8, device="cuda")
+    g_ids, ids = guarded_copy(ids0.astype(np.int32), -77)
+    g_steps, steps = guarded_copy(steps0.astype(np.int32), -77)
+    g_cs, cs = guarded_copy(cs0.astype(np.uint8), 0xA5)
+    g_nm, n_masked = guarded(B, torch.int32, -77)
+    g_conf, conf = guarded(B * S, torch.float32, float("nan"))
+    g_com, commit = guarded(B * S, torch.uint8, 0xA5)
+    conf.fill_(-1.0)
+    commit.fill_(7)
     tt.tt_confidence_unmask(d_logits, ids, steps, B, S, V, mask_id, gamma, T, n_masked=n_masked,
                             conf=conf, commit=commit, commit_step=cs)
     torch.cuda.synchronize()
-    return dict(ids=host(ids), steps=host(steps), n_masked=host(n_masked), conf=host(conf),
-                commit=host(commit), commit_step=host(cs))
+    for full, fill, name in ((g_ids, -77, "ids"), (g_steps, -77, "steps"), (g_cs, 0xA5, "commit_step"),
+                             (g_nm, -77, "n_masked"), (g_conf, float("nan"), "conf"),
+                             (g_com, 0xA5, "commit")):
+        check_guards(full, fill, name)
+    return dict(ids=host(ids), steps=host(steps), n_masked=host(n_masked), conf=host(conf).reshape(B, S),
+                commit=host(commit).reshape(B, S), commit_step=host(cs))
 
 
 def _abs_bound(hr, W, rows=16384):
@@ -217,22 +316,22 @@ def compare_lmhead(gpu, h, W, ids0, steps0, cs0, mask, kind, gamma, T, tau, seqs
                 if c_sorted[k - 1] - c_sorted[k] <= 2 * tol.max() * c_sorted[k - 1]:
                     ambiguous = True
         com = gpu["commit"][b].astype(bool)
-        # validity (every sequence): commits only at masked positions, decoded ones kept,
-        # each committed token within 2 delta of the top logit, the rest still masked
-        assert np.all(~com | masked)
-        assert np.array_equal(gpu["ids"][b][~masked], ids0[b][~masked])
-        assert np.all(gpu["ids"][b][masked & ~com] == mask)
+        # validity (every sequence): each committed token within 2 delta of the top
+        # logit (the oracle's argmax itself unless the top two are that close), and the
+        # commit set one that the sampler's rule allows given the confidence tolerance
+        tok_ok = r["tok"].copy()
         for j, p_ in enumerate(pos):
             if com[p_]:
                 t = gpu["ids"][b][p_]
                 assert t != mask and lg[j, t] >= srt[j, -1] - 2 * delta[j], f"b={b} pos={p_}: token {t}"
+                if near_tie[j]:
+                    tok_ok[p_] = t
         assert gpu["steps"][b] == r["steps"]
-        if kind == 1:
-            assert com.sum() == 1
-        elif kind == 2:
-            assert com.sum() == r["k_min"]
-        else:
-            assert com.sum() >= r["k_min"]
+        band = np.zeros(S)
+        band[pos] = tol * co
+        check_decision_validity(gpu["ids"][b], com, ids0[b], tok_ok, r["conf"], mask, kind, gamma,
+                                r["k_min"], band, what=f"b={b}")
+        assert gpu["n_masked"][b] == pos.size - int(com.sum()), f"b={b}: n_masked"
         if ambiguous:
             excluded += 1
             continue

@@ -222,3 +222,9 @@ def test_sampler_unmask_validation():
     assert call(tt.tt_sampler(0, 0.8, float("inf"), 16)) == tt.TT_ERR_INVALID_ARG
     assert call(tt.tt_sampler(1, 0.8, 1.0, 16), mask=1024) == tt.TT_ERR_INVALID_ARG
     assert call(tt.tt_sampler(2, 0.8, 1.0, 16), V=1022) == tt.TT_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("limit_us", [0, 1000001])
+def test_selftest_wait_limit_rejected(limit_us):
+    assert tt.lib.tt_selftest_wait_timeout(limit_us, None) == tt.TT_ERR_INVALID_ARG
+    assert "limit_us" in tt.lib.tt_last_error().decode()

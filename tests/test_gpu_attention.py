@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from block_wise_mask_tt_b300 import synth
-from gpu_util import bf16_to_f64, check_attention, dev, host
+from gpu_util import bf16_to_f64, check_attention, check_guards, dev, guarded, host
 
 pytestmark = pytest.mark.gpu
 
@@ -32,13 +32,17 @@ def run_attn(tt, w, inp, num_splits=0):
         kc = dev(inp["k_ctx"]) if L else None
         vc = dev(inp["v_ctx"]) if L else None
         pt = None
-    out = torch.full((B, S, Hq, D), 0x7FC0, dtype=torch.int16, device="cuda")  # NaN pattern
-    lse = torch.full((B, S, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    # outputs between canaries (bf16 NaN pattern / NaN) that must come back untouched
+    g_out, out = guarded(B * S * Hq * D, torch.int16, 0x7FC0)
+    g_lse, lse = guarded(B * S * Hq, torch.float32, float("nan"))
     tt.tt_denoise_attn(dims, dev(inp["q"]), dev(inp["k_blk"]), dev(inp["v_blk"]), kc, vc, pt,
                        dev(inp["ctx_len"]), out, lse)
     torch.cuda.synchronize()
     assert tt.tt_device_status(True) == 0
-    return bf16_to_f64(host(out)), host(lse).astype(np.float64)
+    check_guards(g_out, 0x7FC0, "out")
+    check_guards(g_lse, float("nan"), "lse")
+    return (bf16_to_f64(host(out)).reshape(B, S, Hq, D),
+            host(lse).astype(np.float64).reshape(B, S, Hq))
 
 
 def W(**kw):

@@ -162,6 +162,8 @@ def test_lmhead_full_vocabulary(tt, B):
     seqs = [0] if B == 1 else [0, 13, 31]
     excl = compare(gpu, h, W, ids0, np.zeros(B, np.int32), np.zeros((B, S), np.uint8), mask, CONFIDENCE,
                    0.8, S, 1.0, seqs=seqs)
-    assert excl < len(seqs) or len(seqs) == 1
+    # every sampled sequence was checked for validity in full; at least one of the
+    # batched ones also bit for bit
+    assert B == 1 or excl < len(seqs)
     # every sequence took one step and committed at least one position
     assert np.all(gpu["steps"] == 1) and np.all(gpu["commit"].sum(1) >= 1)

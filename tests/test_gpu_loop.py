@@ -14,7 +14,8 @@ import torch
 
 import oracle
 from block_wise_mask_tt_b300 import synth
-from gpu_util import (adaln_tol, bf16_to_f64, check_attention, compare_unmask, dev, host)
+from gpu_util import (adaln_tol, bf16_to_f64, check_attention, compare_unmask, dev, host,
+                      record_excluded)
 
 pytestmark = pytest.mark.gpu
 
@@ -89,6 +90,7 @@ def test_step_by_step_teacher_forced_then_graph_loop(tt, name):
     B, S, T, mask = w.B, w.S, w.steps_max, w.mask_id
     O_ref, _ = oracle.denoise_attention(lp.inp, w.softmax_scale)
     excluded = 0
+    decisions = 0
     n_steps = 0
     for k in range(T + 1):
         ids0 = host(lp.t["ids"]).copy()
@@ -119,6 +121,7 @@ def test_step_by_step_teacher_forced_then_graph_loop(tt, name):
             gpu["conf"][b] = 0.0
             gpu["commit"][b] = 0
         excluded += compare_unmask(gpu, ora, ids0, steps0, mask, w.gamma, what=f"{name} step {k}")
+        decisions += int(active.sum())
         # adaLN of the active sequences uses table row n_masked (t = n_masked / S)
         y = bf16_to_f64(host(lp.t["y"]))
         for b in np.flatnonzero(active):
@@ -128,6 +131,7 @@ def test_step_by_step_teacher_forced_then_graph_loop(tt, name):
             assert np.all(np.abs(y[b] - ref) <= adaln_tol(ref, sh))
         O = bf16_to_f64(host(lp.t["attn_out"]))
         check_attention(O[active], O_ref[active], what=f"{name} step {k}")
+    record_excluded(f"reduced loop {name}", excluded, decisions)
     final = (host(lp.t["ids"]).copy(), host(lp.t["steps"]).copy(), host(lp.t["commit_step"]).copy())
     assert np.all(final[0] != mask)
     assert np.all(final[1] <= T) and n_steps <= T

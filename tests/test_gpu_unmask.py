@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 from block_wise_mask_tt_b300 import synth
-from gpu_util import compare_unmask, oracle_unmask_batch, run_unmask
+from gpu_util import compare_unmask, oracle_unmask_batch, record_excluded, run_unmask
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,8 @@ def test_unmask_matches_oracle(tt, case):
         ids0, steps0, cs0 = _state(B, S, mask, seed, frac, max_step=max(0, min(T - 1, 3)))
         gpu = run_unmask(tt, logits, ids0, steps0, cs0, mask, gamma, T)
         ora = oracle_unmask_batch(logits, ids0, steps0, cs0, mask, gamma, T)
-        compare_unmask(gpu, ora, ids0, steps0, mask, gamma, what=f"seed {seed}")
+        n = compare_unmask(gpu, ora, ids0, steps0, mask, gamma, what=f"seed {seed}")
+        record_excluded(f"unmask B{B} S{S} V{V} gamma={gamma}", n, B)
 
 
 def test_ties_and_mask_id(tt):

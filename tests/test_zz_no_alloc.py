@@ -7,8 +7,11 @@ scratch in a fixed array inside the library instead.  These tests call it throug
 the C ABI and compare it with tt_confidence_unmask (which takes a workspace) on the
 same inputs, using the parity rules of the other unmask tests: token ids, commit
 masks, step counts and commit steps bit-exact, confidences within 1e-5 relative.
-Two calls in a row are checked, the second with a smaller batch, so stale contents
-left in the shared scratch by the first call would show.
+Two calls in a row are checked.  The first (12 sequences at V = 131072) fills the
+front of the scratch with its per-chunk partial results; the second (5 sequences at
+V = 8192) is smaller, so its completion counters fall on words the first call left
+non-zero: the second call decides correctly only if the entry point clears them.
+Both calls are also compared directly with the oracle's unmask step.
 
 This file is named to be collected last.
 """
@@ -16,8 +19,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from block_wise_mask_tt_b300 import synth
-from gpu_util import CONF_REL, dev, host
+from gpu_util import CONF_REL, compare_unmask, dev, host
 
 
 @pytest.fixture(scope="module")
@@ -62,26 +66,41 @@ def _same(a, b, what):
     assert np.array_equal(a["conf"][~m], b["conf"][~m]), f"{what}: conf of decoded positions"
 
 
+def _oracle(w, lg, ids0, steps0, got, what):
+    """The oracle's unmask step of every sequence from the same state and the same
+    host-generated logits."""
+    ora = [oracle.unmask_step(lg[b], ids0[b], int(steps0[b]), w.mask_id, w.gamma, w.steps_max,
+                              np.zeros(w.S, np.uint8)) for b in range(ids0.shape[0])]
+    compare_unmask(got, ora, ids0, steps0, w.mask_id, w.gamma, what=what)
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(tt):
-    w = synth.BATCHED.replace(B=12, V=32768)
+    w = synth.BATCHED.replace(B=12)
     rng = np.random.default_rng(7)
-    # call 1: 12 sequences, some positions already decoded
+    # call 1: 12 sequences at V = 131072, some positions already decoded
     ids0 = np.full((w.B, w.S), w.mask_id, np.int64)
-    ids0[rng.random((w.B, w.S)) < 0.3] = 11
+    # some positions of the first four sequences already decoded; the later rows stay
+    # masked, so their chunk partials (scratch bytes 8192 .. 24575) are all written
+    ids0[:4][rng.random((4, w.S)) < 0.3] = 11
     steps0 = rng.integers(0, 4, w.B)
-    lg = dev(_logits(w, w.B, steps0, ids0, seed=1, block=0))
+    lg_h = _logits(w, w.B, steps0, ids0, seed=1, block=0)
+    lg = dev(lg_h)
     ref = _run(tt, tt.tt_confidence_unmask, lg, ids0, steps0, w)
     got = _run(tt, tt.tt_confidence_unmask_noalloc, lg, ids0, steps0, w)
     _same(got, ref, "call 1")
-    # call 2, straight after: fewer sequences and a larger vocabulary, from the state
-    # call 1 produced
-    w2 = w.replace(B=5, V=131072)
+    _oracle(w, lg_h, ids0, steps0, got, "call 1")
+    # call 2, straight after: fewer sequences and a smaller vocabulary, from the state
+    # call 1 produced; its counters (scratch bytes 11520 .. 11859) sit where call 1
+    # left partial results
+    w2 = w.replace(B=5, V=8192)
     ids1, steps1 = ref["ids"][:5].astype(np.int64), ref["steps"][:5]
-    lg2 = dev(_logits(w2, w2.B, steps1, ids1, seed=1, block=0))
+    lg2_h = _logits(w2, w2.B, steps1, ids1, seed=2, block=0)
+    lg2 = dev(lg2_h)
     ref2 = _run(tt, tt.tt_confidence_unmask, lg2, ids1, steps1, w2)
     got2 = _run(tt, tt.tt_confidence_unmask_noalloc, lg2, ids1, steps1, w2)
     _same(got2, ref2, "call 2")
+    _oracle(w2, lg2_h, ids1, steps1, got2, "call 2")
     assert ref2["commit"].sum() > 0
 
 
