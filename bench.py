@@ -71,6 +71,9 @@ def parse_args():
                     help="profiling aid: run only --reps standalone calls of one entry point on "
                          "the workload (after 3 untimed ones) and print their mean time")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--attn-splits", type=int, default=0,
+                    help="context splits per (sequence, kv head) of the attention; 0 = the "
+                         "library's choice (a sweep aid for the split cost model)")
     ap.add_argument("--lm-head", action="store_true",
                     help="the step's logits come from the fused LM head over the adaLN output "
                          "(synthetic projection W [V][H]) instead of the hash stand-in")
@@ -243,7 +246,8 @@ class Workbench:
     """Device-resident inputs, state and buffers for one replica of the workload."""
 
     def __init__(self, tt, torch, w: synth.Workload, seed: int, sampler: int = 0,
-                 temperature: float = 1.0, lm_head: bool = False, qkv_proj: bool = False):
+                 temperature: float = 1.0, lm_head: bool = False, qkv_proj: bool = False,
+                 attn_splits: int = 0):
         self.tt, self.torch, self.w, self.seed = tt, torch, w, seed
         self.lm_head = lm_head
         self.qkv_proj = qkv_proj
@@ -258,11 +262,12 @@ class Workbench:
         if w.paged:
             kp = self.inp["k_pages"]
             self.dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, 0, w.page_size,
-                                     self.inp["page_table"].shape[1], kp.shape[0], w.softmax_scale, 0)
+                                     self.inp["page_table"].shape[1], kp.shape[0], w.softmax_scale,
+                                     attn_splits)
             kc, vc, pt = dev(kp), dev(self.inp["v_pages"]), dev(self.inp["page_table"])
         else:
             self.dims = tt.attn_dims(B, S, w.Hq, w.Hkv, w.D, self.inp["k_ctx"].shape[1], 0, 0, 0,
-                                     w.softmax_scale, 0)
+                                     w.softmax_scale, attn_splits)
             kc, vc, pt = dev(self.inp["k_ctx"]), dev(self.inp["v_ctx"]), None
         T = torch
         self.t = dict(
@@ -815,7 +820,7 @@ def measure_workload(args, tt, torch, w, seed, flush, world, dist, smi_id, legs:
     """Steps/s of one workload (timed whole blocks), its standalone kernel times and
     rooflines, and the end-to-end figure through host buffers."""
     wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
-                   args.qkv_proj)
+                   args.qkv_proj, args.attn_splits)
     warm_plan = plan_blocks(wb, 100_000, max(args.warmup, 3))
     plan = plan_blocks(wb, 0, args.steps)
     total_steps = sum(t for _, _, t in plan)
@@ -903,7 +908,7 @@ def main():
     seed = replica_seed(args.seed, rank)
     if args.kernel_only:
         wb = Workbench(tt, torch, w, seed, SAMPLERS[args.sampler], args.temperature, args.lm_head,
-                       args.qkv_proj)
+                       args.qkv_proj, args.attn_splits)
         kernel_only(wb, args.kernel_only, args.reps)
         return
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")

@@ -203,18 +203,18 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
         g.max_ctx = 0;
         g.page_size = 0;
     }
-    const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
-    size_t acc_bytes = rows * g.D * sizeof(float);
-    acc_bytes = (acc_bytes + 255) & ~size_t(255);
-    float* part_acc = static_cast<float*>(ws);
-    float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-    // Epilogue store maps: partial states when the context is split, else the output
-    // itself (when G divides 128, so that a 128-row tile covers whole positions).
+    float* part_acc = nullptr;
+    float* part_ml = nullptr;
+    unsigned* ticket = nullptr;
+    tti::attn_layout(g, ws, &part_acc, &part_ml, &ticket);
+    // Epilogue store maps: partial states when the context is split and a second pass
+    // combines them; the output itself wherever a CTA may write it directly (when G
+    // divides 128, so that a 128-row tile covers whole positions).
     tti::AttnMaps maps = pl.maps;
-    maps.part = maps.kb;  // placeholders for the map that is not used
+    maps.part = maps.kb;  // placeholders for the maps that are not used
     maps.out = maps.kb;
     maps.out_tma = 0;
-    if (g.n_splits > 1) {
+    if (g.n_splits > 1 && !g.inline_merge) {
         const cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.R,
                                     (cuuint64_t)g.B * g.Hkv * g.n_splits};
         const cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)g.R * g.D * 4};
@@ -236,11 +236,12 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     sp.skip_if_zero = skip_if_zero;
     sp.part_acc = part_acc;
     sp.part_ml = part_ml;
+    sp.ticket = ticket;
     sp.out = static_cast<uint16_t*>(out);
     sp.lse = lse;
     sp.err = err;
     TT_CUDA(tti::launch_attn_split(sp, maps, st));
-    if (g.n_splits > 1) {
+    if (g.n_splits > 1 && !g.inline_merge) {
         tti::AttnMergeParams mp;
         mp.g = g;
         mp.ctx_len = sp.ctx_len;

@@ -150,13 +150,17 @@ struct AttnGeom {
     int page_size;     // 0 or 64
     int max_pages, num_pages;
     int n_splits;
-    int tiles_per_split;  // 64-token tiles per split
+    int tiles_per_split;  // 128-token tiles per split
+    int inline_merge;     // 1: the last split CTA of a row group merges (n_splits <= 4)
     float scale_log2;     // softmax_scale * log2(e)
 };
+constexpr int kAttnInlineMergeMax = 4;  // most splits the split kernel merges itself
 bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_size,
                    int max_pages, int num_pages, float softmax_scale, int num_splits,
                    AttnGeom& g, const char** why);
 size_t attn_workspace_bytes(const AttnGeom& g);
+// Pointers into a workspace of attn_workspace_bytes(g) bytes.
+void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket);
 
 struct AttnSplitParams {
     AttnGeom g;
@@ -166,7 +170,9 @@ struct AttnSplitParams {
     const int32_t* skip_if_zero; // nullable
     float* part_acc;             // [B][Hkv][n_splits][R][D]
     float* part_ml;              // [B][Hkv][n_splits][R][2]
-    uint16_t* out;               // bf16 [B][S][Hq][D]: written here when n_splits == 1
+    unsigned int* ticket;        // [B][Hkv][n_rg]: zero on entry and on exit (inline merge)
+    uint16_t* out;               // bf16 [B][S][Hq][D]: written here when n_splits == 1 or
+                                 // when the split kernel merges (inline_merge)
     float* lse;                  // nullable, [B][S][Hq]: likewise
     int* err;
 };

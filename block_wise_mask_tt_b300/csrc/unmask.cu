@@ -66,9 +66,12 @@ __global__ void __launch_bounds__(kThreads, 6) unmask_kernel(UnmaskParams p) {
                     x[4 * u + 2] = q[u].z;
                     x[4 * u + 3] = q[u].w;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        id[4 * u + e] = i0 + e;
-                        if (i0 + e == mid) x[4 * u + e] = -CUDART_INF_F;
+                    for (int e = 0; e < 4; ++e) id[4 * u + e] = i0 + e;
+                    // the mask id lies in at most one vector of the row: one test per vector
+                    if ((unsigned)(mid - i0) < 4u) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (i0 + e == mid) x[4 * u + e] = -CUDART_INF_F;
                     }
                 }
                 fold<4 * kBatch>(acc, x, id, p.temp_scale);

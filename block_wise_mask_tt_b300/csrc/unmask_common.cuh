@@ -53,7 +53,9 @@ __device__ __forceinline__ Red warp_combine(Red v, float ts) {
 // triple of this thread.  The batch maximum comes from a 3-input max tree; its id is
 // looked for only when it beats the running maximum (rare once a row's first batches
 // are in), and an equal maximum keeps the running, lower id.  The exponentials use one
-// packed FMA per pair and a packed running sum.
+// packed FMA per pair, the SFU's 2^x (relative error about 2^-22, results below 2^-126
+// flushed to zero: terms that small cannot move a sum that holds the maximum's 1) and
+// a packed running sum.
 template <int N>
 __device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&id)[N], float ts) {
     static_assert(N % 2 == 0, "pairs");
@@ -78,7 +80,7 @@ __device__ __forceinline__ void fold(Red& acc, const float (&x)[N], const int (&
     for (int i = 0; i < N; i += 2) {
         float e0, e1;
         ttk::f2_unpack(ttk::f2_fma(ttk::f2_pack(x[i], x[i + 1]), ts2, off2), e0, e1);
-        s2 = ttk::f2_add(s2, ttk::f2_pack(exp2f(e0), exp2f(e1)));
+        s2 = ttk::f2_add(s2, ttk::f2_pack(ttk::ex2_ftz(e0), ttk::ex2_ftz(e1)));
     }
     float s0, s1;
     ttk::f2_unpack(s2, s0, s1);

@@ -29,7 +29,7 @@ def test_exports_every_header_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert tt.tt_abi_version() == 3
+    assert tt.tt_abi_version() == 4
     names = [tt.lib.tt_status_string(i).decode() for i in range(7)]
     assert names == ["TT_OK", "TT_ERR_INVALID_ARG", "TT_ERR_UNSUPPORTED", "TT_ERR_CUDA",
                      "TT_ERR_DEVICE", "TT_ERR_TIMEOUT", "TT_ERR_WORKSPACE"]

@@ -124,13 +124,17 @@ def test_block_permutation_equivariance(tt):
     np.testing.assert_allclose(O2, O[:, perm], atol=2e-2, rtol=0)
 
 
-def test_bad_page_id_is_reported(tt):
-    w = W(B=2, L=200, L_min=1, S=16, Hq=8, Hkv=2, D=64, paged=True, softmax_scale=0.125)
-    inp = synth.make_attention_inputs(w, seed=14)
+@pytest.mark.parametrize("splits", [0, 2, 6])
+def test_bad_page_id_is_reported(tt, splits):
+    """A page id outside the pool sets the error word and skips that sequence's
+    context, whether the CTA writes the output itself, merges the splits itself (2) or
+    leaves them to the combine pass (6); the other sequence is unaffected."""
+    w = W(B=2, L=700, L_min=1, S=16, Hq=8, Hkv=2, D=64, paged=True, softmax_scale=0.125)
+    inp = synth.make_attention_inputs(w, seed=14, ctx_len=np.array([650, 700], np.int32))
     inp["page_table"][1, 0] = 10 ** 6
     kp = inp["k_pages"]
     dims = tt.attn_dims(w.B, w.S, w.Hq, w.Hkv, w.D, 0, 64, inp["page_table"].shape[1], kp.shape[0],
-                        w.softmax_scale, 0)
+                        w.softmax_scale, splits)
     out = torch.zeros((w.B, w.S, w.Hq, w.D), dtype=torch.int16, device="cuda")
     assert tt.tt_device_status(True) == 0
     tt.tt_denoise_attn(dims, dev(inp["q"]), dev(inp["k_blk"]), dev(inp["v_blk"]), dev(kp),
