@@ -14,19 +14,19 @@
 //     front of its context tiles, so the block keys run on the tensor cores too;
 //   * warp 0 streams 128-token K/V tiles (two 64-row TMA boxes each, so a tile may
 //     span two pages of a paged cache) into a shared-memory ring with 128-byte
-//     swizzle; warp 1 issues every tcgen05.mma; four softmax warpgroups share the
-//     rows: warpgroup q takes keys 32q .. 32q+31 of every 128-key tile for all 128
-//     rows of a row tile (one row per thread / TMEM lane), tile 0 and then tile 1, so
-//     each tile's softmax runs on all 16 softmax warps.  The four quarters of a row
-//     agree on its max through shared memory and a named barrier;
+//     swizzle; warp 1 issues every tcgen05.mma; four softmax warpgroups own the rows:
+//     warpgroup (i, h) takes tile i's 128 rows (one per thread / TMEM lane) and keys
+//     64h .. 64h+63 of every 128-key tile.  The two halves of a row agree on its max
+//     through shared memory and a named barrier;
 //   * Q sits in shared memory for the whole CTA; the scores S go to tensor memory
 //     (TMEM); the softmax turns them into P = exp2(S*scale*log2e - m) (bf16) written
-//     back over the front of each quarter's S columns, which is the TMEM A operand of
-//     PV; O accumulates in TMEM.  N = 128 keys per QK^T instruction keeps the tensor
-//     core near its peak rate (64-key products run at little more than half of it);
+//     back over the front of each half's S columns, which is the TMEM A operand of
+//     PV; O accumulates in
+//     TMEM.  N = 128 keys per QK^T instruction keeps the tensor core near its peak
+//     rate (64-key products run at little more than half of it);
 //   * the two row tiles ping-pong: the MMA warp issues QK(0,j) QK(1,j) | PV(0,j)
-//     QK(0,j+1) | PV(1,j) QK(1,j+1) | ..., so one tile's softmax overlaps the other
-//     tile's matrix products;
+//     QK(0,j+1) | PV(1,j) QK(1,j+1) | ..., so one tile's softmax overlaps the other's
+//     matrix products;
 //   * the running max is raised (and O rescaled in TMEM) only when it grows by more
 //     than 2^8, so most tiles need no correction;
 //   * with a single split the CTA writes the normalised output (bf16) and the lse
@@ -55,24 +55,17 @@ struct Cfg {
     static constexpr int NP = D / 64;                      // 128-byte column parts of a row
     static constexpr uint32_t kPart = kTileKeys * 128;     // 128 rows x 128 B (one part of a tile)
     static constexpr uint32_t kTile = NP * kPart;          // one K (or V) tile
-    // Ring depths.  Under a full-GPU stream a TMA tile takes ~5000 cycles to land, so
-    // about 90 KB per SM must be in flight; K is needed earlier in a round than V
-    // (QK^T of the next tile is issued right after PV of this one), so K gets the
-    // deeper ring: D = 128 holds 3 K and 2 V tiles (160 KiB) next to the Q tiles.
-    static constexpr int kStagesK = (D == 128) ? 3 : 4;
-    static constexpr int kStagesV = (D == 128) ? 2 : 4;
+    static constexpr uint32_t kStage = 2 * kTile;          // K then V
+    static constexpr int kStages = (D == 128) ? 2 : 4;     // K/V ring depth (128 KiB)
     static constexpr uint32_t kQPart = 128 * 128;          // 128 query rows x 128 B
     static constexpr uint32_t kQTile = NP * kQPart;        // one 128-row Q tile
-    static constexpr uint32_t kRing = 2 * kQTile;          // Q tiles first, then the K ring
-    static constexpr uint32_t kRingV = kRing + kStagesK * kTile;  // then the V ring
-    // After every MMA has completed the V ring is idle: the four quarters' row sums
-    // are exchanged there (float [2 tiles][4 quarters][128]); the epilogue staging
-    // below it ends before the V ring starts.
-    static constexpr uint32_t kLx = kRingV;
-    static constexpr uint32_t kBar = kRingV + kStagesV * kTile;
-    // mbarriers: k_full[kStagesK], k_empty[kStagesK], v_full[kStagesV], v_empty[kStagesV],
-    // s_full[2], p_full[2], o_full, q_ready; then the TMEM slot.
-    static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 6;
+    static constexpr uint32_t kRing = 2 * kQTile;          // Q tiles first, then the ring
+    static constexpr uint32_t kXchg = kRing + kStages * kStage;  // float [2 tiles][2 halves][128]
+    static constexpr uint32_t kBar = kXchg + 2 * 2 * 128 * 4;
+    // mbarriers: k_full[st], v_full[st], k_empty[st], v_empty[st], s_full[2], p_full[2],
+    // o_full, q_ready; then the TMEM slot.  K and V of a stage are tracked apart: K is
+    // free again once both QK^T products have read it, a round before V.
+    static constexpr int kNumBars = 4 * kStages + 6;
     static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
     static constexpr uint32_t kEnd = kSlot + 16;
     static constexpr uint32_t kBytes = kEnd + 1024;        // alignment slack
@@ -80,115 +73,26 @@ struct Cfg {
     // O_i at 256 + D i.
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColO = 256;
-    // Epilogue staging without a tensor map: one quarter row (D/4 bf16) per softmax
-    // thread and tile, padded so the 16-byte stores of consecutive rows fall in
-    // different banks.
-    static constexpr uint32_t kQuarterRow = D / 2 + 16;
+    // Epilogue staging: one half row (D/2 floats) per softmax thread, padded so the
+    // 16-byte stores of consecutive rows fall in different banks.
+    static constexpr uint32_t kHalfRow = D * 2 + 16;
     static_assert(kColO + 2 * D <= 512, "TMEM budget");
     static_assert(kBytes <= 227 * 1024, "shared memory budget");
-    static_assert(256 * 4 * kQuarterRow <= kLx, "epilogue staging ends before the row-sum exchange");
-    static_assert(2 * (D / 32) * 16384 <= kLx, "tensor-store staging ends before the row-sum exchange");
-    static_assert(2 * 4 * 128 * 4 <= kStagesV * kTile, "row-sum exchange fits in the V ring");
+    static_assert(512 * kHalfRow <= kXchg, "epilogue staging fits in the Q tiles + ring");
 };
+
+__device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
+}
 
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Ticket increment with acquire-release semantics at GPU scope: the partial states this
-// CTA stored (ordered before it by the fence and barrier in arrive_and_merge) are
-// released, and the arrival that sees the final count acquires every earlier one.
-__device__ __forceinline__ unsigned ticket_add(unsigned* t) {
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
-    return old;
-}
-__device__ __forceinline__ unsigned ticket_acquire(const unsigned* t) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(t) : "memory");
-    return v;
-}
-
-// Combines the partial states (m, l, O) of the nv non-empty splits of row group
-// (b, gkv, rg) into the bf16 output and the lse.  Threads t = 0 .. nthr-1 of the
-// caller share the (row, column quarter) items; consecutive threads take the four
-// quarters of one row, so a warp reads eight whole 512-byte rows at a time.
-template <int D>
-__device__ void merge_group(const AttnSplitParams& p, int b, int gkv, int rg, int nv, int t, int nthr) {
-    const AttnGeom& g = p.g;
-    constexpr int QC = D / 4;  // columns of one work item
-    for (int w = t; w < 256 * 4; w += nthr) {
-        const int r = w >> 2, qq = w & 3;
-        const int r_glob = rg * 256 + r;
-        if (r >= g.rows_per_cta || r_glob >= g.R) continue;
-        const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + r_glob;
-        float ms[kAttnInlineMergeMax], ls[kAttnInlineMergeMax];
-        float mx = -CUDART_INF_F;
-#pragma unroll
-        for (int c = 0; c < kAttnInlineMergeMax; ++c) {
-            ms[c] = -CUDART_INF_F;
-            ls[c] = 0.f;
-            if (c < nv) {
-                const size_t pi = base + (size_t)c * g.R;
-                ms[c] = __ldcg(p.part_ml + 2 * pi);
-                ls[c] = __ldcg(p.part_ml + 2 * pi + 1);
-                mx = fmaxf(mx, ms[c]);
-            }
-        }
-        float acc[QC];
-#pragma unroll
-        for (int e = 0; e < QC; ++e) acc[e] = 0.f;
-        float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < kAttnInlineMergeMax; ++c) {
-            // an empty partial state (m = -inf) has weight 0 and is not read
-            if (c >= nv || ms[c] == -CUDART_INF_F) continue;
-            const float wc = exp2f(ms[c] - mx);
-            lsum = fmaf(wc, ls[c], lsum);
-            const float4* ap = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * g.R) * D + qq * QC);
-#pragma unroll
-            for (int e = 0; e < QC / 4; ++e) {
-                const float4 v = __ldcg(ap + e);
-                acc[4 * e + 0] = fmaf(wc, v.x, acc[4 * e + 0]);
-                acc[4 * e + 1] = fmaf(wc, v.y, acc[4 * e + 1]);
-                acc[4 * e + 2] = fmaf(wc, v.z, acc[4 * e + 2]);
-                acc[4 * e + 3] = fmaf(wc, v.w, acc[4 * e + 3]);
-            }
-        }
-        const float inv = 1.0f / lsum;
-        const int s = r_glob / g.G, jh = r_glob % g.G;
-        const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh;
-        uint4* op = reinterpret_cast<uint4*>(p.out + orow * D + qq * QC);
-#pragma unroll
-        for (int e = 0; e < QC / 8; ++e) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const __nv_bfloat162 pr =
-                    __floats2bfloat162_rn(acc[8 * e + 2 * u] * inv, acc[8 * e + 2 * u + 1] * inv);
-                w4[u] = *reinterpret_cast<const uint32_t*>(&pr);
-            }
-            op[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        if (qq == 0 && p.lse != nullptr) p.lse[orow] = (mx + log2f(lsum)) * kLn2;
-    }
-}
-
-// Called by threads t = 0 .. nthr-1 of a split CTA once its partial state is stored:
-// counts the split in on the row group's ticket; the split that arrives last merges
-// all of them and leaves the ticket at zero.  bar_id 0 is __syncthreads (nthr = the
-// whole CTA), otherwise a named barrier over nthr threads.
-template <int D>
-__device__ void arrive_and_merge(const AttnSplitParams& p, int item, int b, int gkv, int rg, int nv, int t,
-                                 int nthr, uint32_t* flag_slot, int bar_id) {
-    __threadfence();  // this thread's partial-state stores, before the arrival below
-    if (bar_id == 0) __syncthreads(); else named_sync(bar_id, nthr);
-    if (t == 0) *flag_slot = (ticket_add(p.ticket + item) == (unsigned)(nv - 1)) ? 1u : 0u;
-    if (bar_id == 0) __syncthreads(); else named_sync(bar_id, nthr);
-    if (*flag_slot == 0u) return;
-    (void)ticket_acquire(p.ticket + item);  // every merging thread sees every split's stores
-    merge_group<D>(p, b, gkv, rg, nv, t, nthr);
-    if (t == 0) p.ticket[item] = 0u;
 }
 
 template <int D>
@@ -199,8 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ttk::pdl_trigger();
     using C = Cfg<D>;
     constexpr int NP = C::NP;
-    constexpr int NSK = C::kStagesK;
-    constexpr int NSV = C::kStagesV;
+    constexpr int NS = C::kStages;
     constexpr uint32_t kIdescQK = ttk::idesc_bf16(128, kTileKeys, false, false);
     constexpr uint32_t kIdescPV = ttk::idesc_bf16(128, D, false, true);
 
@@ -208,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kSlot);
-    float* lx = reinterpret_cast<float*>(smem + C::kLx);  // row sums [tile][quarter][row], at the end
+    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // [tile][half][row]
 
     const AttnGeom& g = p.g;
     const int tid = threadIdx.x;
@@ -216,10 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Grid: x = row group item (rg fastest, then kv head, then sequence), y = split.
     // Splits vary slowest, so on a ragged batch the short last splits of long
     // sequences are dispatched last and the tail of the grid is short.
-    const int item = blockIdx.x;
-    const int rg = item % g.n_rg;
-    const int gkv = (item / g.n_rg) % g.Hkv;
-    const int b = item / (g.n_rg * g.Hkv);
+    const int rg = blockIdx.x % g.n_rg;
+    const int gkv = (blockIdx.x / g.n_rg) % g.Hkv;
+    const int b = blockIdx.x / (g.n_rg * g.Hkv);
     const int split = blockIdx.y;
 
     if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return;
@@ -238,11 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = nblk + max(0, t1 - t0);
     if (nt == 0) return;  // this split is empty; the combine pass does not read it
     const int n_mt = g.n_mt;
-    // Non-empty splits of this row group (split 0 always holds the block's keys).
-    const int nv = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
-    // Direct: this CTA sees every key of its rows and writes the normalised output.
-    const bool direct = g.n_splits == 1 || (g.inline_merge && nv == 1);
-    uint32_t* flag_slot = reinterpret_cast<uint32_t*>(smem + C::kSlot + 4);
+    const bool direct = g.n_splits == 1;
 
     if (g.page_size && t1 > t0) {
         // Every page this split reads must exist; pages past the context end are not read.
@@ -255,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (__syncthreads_or(bad)) {
             // Leave an empty partial state for every row so the combine skips this
-            // split (a direct CTA has no partials: its output is left unwritten).
+            // split (a single-split call has no partials: its output is left unwritten).
             if (tid == 0) ttk::report_error(p.err, ttk::kErrDevice);
             if (!direct) {
                 for (int r = tid; r < g.rows_per_cta; r += kThreads) {
@@ -266,42 +164,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.part_ml[2 * pi + 1] = 0.f;
                     }
                 }
-                if (g.inline_merge) arrive_and_merge<D>(p, item, b, gkv, rg, nv, tid, kThreads, flag_slot, 0);
             }
             return;
         }
     }
 
     const uint32_t sQ = ttk::smem_u32(smem);
-    const uint32_t sRingK = ttk::smem_u32(smem + C::kRing);
-    const uint32_t sRingV = ttk::smem_u32(smem + C::kRingV);
+    const uint32_t sRing = ttk::smem_u32(smem + C::kRing);
     const uint32_t bar0 = ttk::smem_u32(smem + C::kBar);
     auto kfull_bar = [&](int st) { return bar0 + 8u * (uint32_t)st; };
-    auto kempty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(NSK + st); };
-    auto vfull_bar = [&](int st) { return bar0 + 8u * (uint32_t)(2 * NSK + st); };
-    auto vempty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(2 * NSK + NSV + st); };
-    constexpr int kB = 2 * NSK + 2 * NSV;
-    auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kB + i); };
-    auto pfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kB + 2 + i); };
-    const uint32_t ofull_bar = bar0 + 8u * (uint32_t)(kB + 4);
-    const uint32_t qready_bar = bar0 + 8u * (uint32_t)(kB + 5);
+    auto vfull_bar = [&](int st) { return bar0 + 8u * (uint32_t)(NS + st); };
+    auto kempty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(2 * NS + st); };
+    auto vempty_bar = [&](int st) { return bar0 + 8u * (uint32_t)(3 * NS + st); };
+    auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(4 * NS + i); };
+    auto pfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(4 * NS + 2 + i); };
+    const uint32_t ofull_bar = bar0 + 8u * (uint32_t)(4 * NS + 4);
+    const uint32_t qready_bar = bar0 + 8u * (uint32_t)(4 * NS + 5);
 
     if (warp == 1) {
         ttk::tmem_alloc(ttk::smem_u32(tmem_slot), 512);
         ttk::tmem_relinquish();
     }
     if (tid == 0) {
-        for (int st = 0; st < NSK; ++st) {
+        for (int st = 0; st < NS; ++st) {
             ttk::mbar_init(kfull_bar(st), 1);
-            ttk::mbar_init(kempty_bar(st), 1);
-        }
-        for (int st = 0; st < NSV; ++st) {
             ttk::mbar_init(vfull_bar(st), 1);
+            ttk::mbar_init(kempty_bar(st), 1);
             ttk::mbar_init(vempty_bar(st), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ttk::mbar_init(sfull_bar(i), 1);
-            ttk::mbar_init(pfull_bar(i), 512);
+            ttk::mbar_init(pfull_bar(i), 256);
         }
         ttk::mbar_init(ofull_bar, 1);
         ttk::mbar_init(qready_bar, 128 * n_mt * NP);
@@ -312,9 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ttk::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int q = warp / 4 - 1;            // softmax warpgroup 0..3 (its key quarter), or -1
+    const int q = warp / 4 - 1;            // softmax warpgroup 0..3, or -1 for warps 0-3
+    const int mt = q >> 1;                 // its 128-row tile
+    const int half = q & 1;                // its 64 keys of every 128-key tile
     const int lane_row = tid & 127;        // TMEM lane (tile row) of this softmax thread
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int r_local = mt * 128 + lane_row;               // row within this CTA
+    const int r_glob = rg * 256 + r_local;                 // packed row of (b, gkv)
+    const bool in_tile = q >= 0 && mt < n_mt;
+    const bool row_valid = in_tile && r_local < g.rows_per_cta && r_glob < g.R;
 
     bool ok = true;
     if (warp == 0) {
@@ -326,15 +225,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ttk::prefetch_tensormap(&maps.kb);
                 ttk::prefetch_tensormap(&maps.vb);
             }
-            // First cache row of each 64-row half of unit j.  A second half past the end
-            // (the block's S <= 32 keys, or the context end) re-reads the first half's
-            // rows: they are masked out, every box stays in range, and no page past the
-            // sequence is looked up.
-            auto unit_rows = [&](int j, int (&row0)[2]) {
+            int issued[2] = {0, 0};  // K and V tiles whose loads were issued
+            for (int j = 0; j < nt && ok; ++j) {
+                const int st = j % NS;
+                const uint32_t par = (uint32_t)(((j / NS) - 1) & 1);
+                const uint32_t dK = sRing + (uint32_t)st * C::kStage;
+                const bool blk = j < nblk;
                 const int t = t0 + j - nblk;
+                // First cache row of each 64-row half.  A second half past the end (the
+                // block's S <= 32 keys, or the context end) re-reads the first half's
+                // rows: they are masked out, every box stays in range, and no page past
+                // the sequence is looked up.
+                int row0[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (j < nblk) {
+                    if (blk) {
                         row0[h] = b * g.S;
                     } else {
                         const int hh = (t * kTileKeys + h * kSub < ctx) ? h : 0;
@@ -342,54 +247,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               : b * g.max_ctx + t * kTileKeys + hh * kSub;
                     }
                 }
-            };
-            // Loads go out in the order their ring slots free up: K runs up to
-            // NSK - NSV units ahead of V (K(j + NSK) needs QK(1, j) done, V(j + NSV)
-            // needs PV(1, j) done, and QK(1, j) completes before PV(1, j)).
-            auto load = [&](int kv, int j) -> bool {
-                const int ns = kv ? NSV : NSK;
-                const int st = j % ns;
-                if (j >= ns && !ttk::mbar_wait(kv ? vempty_bar(st) : kempty_bar(st), (uint32_t)(((j / ns) - 1) & 1)))
-                    return false;
-                int row0[2];
-                unit_rows(j, row0);
-                const bool blk = j < nblk;
-                const uint32_t fb = kv ? vfull_bar(st) : kfull_bar(st);
-                const uint32_t dst = (kv ? sRingV : sRingK) + (uint32_t)st * C::kTile;
-                const CUtensorMap* map = kv ? (blk ? &maps.vb : &maps.v) : (blk ? &maps.kb : &maps.k);
-                ttk::mbar_arrive_expect_tx(fb, C::kTile);
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int kv = 0; kv < 2; ++kv) {  // K, then V
+                    if (j >= NS && !ttk::mbar_wait(kv ? vempty_bar(st) : kempty_bar(st), par)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = kv ? vfull_bar(st) : kfull_bar(st);
+                    const CUtensorMap* map = kv ? (blk ? &maps.vb : &maps.v) : (blk ? &maps.kb : &maps.k);
+                    ttk::mbar_arrive_expect_tx(fb, C::kTile);
 #pragma unroll
-                    for (int part = 0; part < NP; ++part)
-                        ttk::tma_load_3d(dst + part * C::kPart + h * (kSub * 128), map, part * 64, gkv, row0[h], fb);
-                return true;
-            };
-            int issued[2] = {0, 0};  // K and V tiles whose loads were issued
-            for (int jv = 0; jv < nt && ok; ++jv) {
-                while (ok && issued[0] < nt && issued[0] <= jv + (NSK - NSV)) {
-                    ok = load(0, issued[0]);
-                    if (ok) ++issued[0];
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int part = 0; part < NP; ++part)
+                            ttk::tma_load_3d(dK + kv * C::kTile + part * C::kPart + h * (kSub * 128), map,
+                                             part * 64, gkv, row0[h], fb);
+                    issued[kv] = j + 1;
                 }
-                if (ok) ok = load(1, jv);
-                if (ok) ++issued[1];
             }
             if (!ok) ttk::report_error(p.err, ttk::kErrTimeout);
             // Drain: the most recent loads of every stage must have landed before exit.
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const int ns = kv ? NSV : NSK;
-                for (int st = 0; st < ns && st < issued[kv]; ++st) {
-                    const int jl = st + ((issued[kv] - 1 - st) / ns) * ns;
-                    ttk::mbar_wait(kv ? vfull_bar(st) : kfull_bar(st), (uint32_t)((jl / ns) & 1));
+            for (int kv = 0; kv < 2; ++kv)
+                for (int st = 0; st < NS && st < issued[kv]; ++st) {
+                    const int jl = st + ((issued[kv] - 1 - st) / NS) * NS;
+                    ttk::mbar_wait(kv ? vfull_bar(st) : kfull_bar(st), (uint32_t)((jl / NS) & 1));
                 }
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if ((tid & 31) == 0) {
             auto qk = [&](int i, int j) {
-                const uint32_t sK = sRingK + (uint32_t)(j % NSK) * C::kTile;
+                const uint32_t sK = sRing + (uint32_t)(j % NS) * C::kStage;
                 const uint32_t sQi = sQ + (uint32_t)i * C::kQTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -401,19 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ttk::mma_commit(sfull_bar(i));
             };
             auto pv = [&](int i, int j) {
-                const uint32_t sV = sRingV + (uint32_t)(j % NSV) * C::kTile;
+                const uint32_t sV = sRing + (uint32_t)(j % NS) * C::kStage + C::kTile;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     const uint64_t bd = ttk::sdesc_sw128(sV + k * 2048, C::kPart, 1024);
-                    // keys 16k .. 16k+15: P of key quarter k/2 sits over the front of
-                    // that quarter's own 32 S columns
-                    const uint32_t pcol = C::kColS + 128 * i + 32 * (k >> 1) + 8 * (k & 1);
+                    // keys 16k .. 16k+15: P of key half k/4 sits over the front of that
+                    // half's own 64 S columns
+                    const uint32_t pcol = C::kColS + 128 * i + 64 * (k >> 2) + 8 * (k & 3);
                     ttk::mma_bf16_ts(tmem + C::kColO + i * D, tmem + pcol, bd, kIdescPV,
                                      (j > 0 || k > 0) ? 1u : 0u);
                 }
             };
-            auto wait_k = [&](int j) { return ttk::mbar_wait(kfull_bar(j % NSK), (uint32_t)((j / NSK) & 1)); };
-            auto wait_v = [&](int j) { return ttk::mbar_wait(vfull_bar(j % NSV), (uint32_t)((j / NSV) & 1)); };
+            auto wait_k = [&](int j) { return ttk::mbar_wait(kfull_bar(j % NS), (uint32_t)((j / NS) & 1)); };
+            auto wait_v = [&](int j) { return ttk::mbar_wait(vfull_bar(j % NS), (uint32_t)((j / NS) & 1)); };
             ok = ttk::mbar_wait(qready_bar, 0) && wait_k(0);
             if (ok) {
                 ttk::tc_fence_after();
@@ -431,17 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_k(j + 1))) break;
                     ttk::tc_fence_after();
                     qk(0, j + 1);
-                    if (n_mt == 1) ttk::mma_commit(kempty_bar((j + 1) % NSK));
+                    if (n_mt == 1) ttk::mma_commit(kempty_bar((j + 1) % NS));
                 }
                 if (n_mt == 2) {
                     if (!(ok = ttk::mbar_wait(pfull_bar(1), par))) break;
                     ttk::tc_fence_after();
                     pv(1, j);
                 }
-                ttk::mma_commit(vempty_bar(j % NSV));  // V of tile j is no longer read
+                ttk::mma_commit(vempty_bar(j % NS));  // V of tile j is no longer read
                 if (next && n_mt == 2) {
                     qk(1, j + 1);
-                    ttk::mma_commit(kempty_bar((j + 1) % NSK));
+                    ttk::mma_commit(kempty_bar((j + 1) % NS));
                 }
             }
             if (!ok) ttk::report_error(p.err, ttk::kErrTimeout);
@@ -450,108 +339,108 @@ __global__ void __launch_bounds__(kThreads, 1)
             ttk::mma_commit(ofull_bar);
             ttk::mbar_wait(ofull_bar, 0);
         }
-    } else if (q >= 0) {
-        // ---- Q into shared memory (canonical K-major, 128-B swizzle): warpgroup q loads
-        // 128-byte part (q & 1) of every row of tile (q >> 1) (D = 128: both parts, so
-        // each row arrives in one round trip; D = 64: part 0 alone).
-        {
-            const int qt = q >> 1, qpart = q & 1;
-            if (qt < n_mt && qpart < NP) {
-                const int rl = qt * 128 + lane_row;
-                const int rq = rg * 256 + rl;
-                const bool valid = rl < g.rows_per_cta && rq < g.R;
-                const int s = valid ? rq / g.G : 0, j = valid ? rq % g.G : 0;
-                const uint4* qp = reinterpret_cast<const uint4*>(
-                    p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D) + qpart * 8;
-                uint8_t* qrow = smem + (size_t)qt * C::kQTile + (size_t)qpart * C::kQPart + (size_t)lane_row * 128;
-                uint4 qv[8];
+    } else if (in_tile) {
+        // ---- this row's Q into shared memory (canonical K-major, 128-B swizzle)
+        // Half h loads 128-byte part h of the row (D = 128: both halves, one part
+        // each, so the whole row arrives in one round trip; D = 64: half 0 alone).
+        if (half < NP) {
+            const int s = r_glob / g.G, j = r_glob % g.G;
+            const uint4* qp = reinterpret_cast<const uint4*>(
+                p.q + (((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j) * D) + half * 8;
+            uint8_t* qrow = smem + (size_t)mt * C::kQTile + (size_t)half * C::kQPart + (size_t)lane_row * 128;
+            uint4 qv[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) qv[c] = valid ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < 8; ++c) qv[c] = row_valid ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (lane_row & 7)) << 4)) = qv[c];
-                ttk::fence_proxy_async_smem();
-                ttk::mbar_arrive(qready_bar);
-            }
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (lane_row & 7)) << 4)) = qv[c];
+            ttk::fence_proxy_async_smem();
+            ttk::mbar_arrive(qready_bar);
         }
-        // ---------------------------------------- softmax: key quarter q of every tile
-        // All four warpgroups work on one row tile at a time (tile 0, then tile 1, every
-        // key tile), so a tile's softmax runs on 16 warps while the tensor core works on
-        // the other tile.  Thread (q, lane_row) owns keys 32q .. 32q+31 of row lane_row.
+        // ------------------------------------------------- softmax: tile mt, keys half
+        const uint32_t tS = tmem + lane_off + C::kColS + 128 * mt;
+        const uint32_t tO = tmem + lane_off + C::kColO + mt * D;
         const uint64_t scale2 = ttk::f2_pack(g.scale_log2, g.scale_log2);
-        const int k0 = 32 * q;  // first key of this quarter
-        float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
-        float l_part[2] = {0.f, 0.f};  // sums of p over this quarter's keys
+        float* my_x = xchg + (mt * 2 + half) * 128 + lane_row;
+        const float* other_x = xchg + (mt * 2 + (half ^ 1)) * 128 + lane_row;
+        const int bar_id = 1 + mt;  // named barrier of this tile's two halves
+        float m_run = -CUDART_INF_F;
+        float l_part = 0.f;  // sum of p over this half's keys
         for (int j = 0; j < nt; ++j) {
+            // A wait that runs out is recorded, but the loop goes on: every thread of
+            // the tile must reach the named barriers below the same number of times.
+            // (After a missed phase the later parity waits return at once.)
+            if (!ttk::mbar_wait(sfull_bar(mt), (uint32_t)(j & 1))) ok = false;
+            ttk::tc_fence_after();
             const int lim = (j < nblk) ? g.S : ctx - (t0 + j - nblk) * kTileKeys;  // keys >= lim lie outside
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt >= n_mt) break;
-                const uint32_t tS = tmem + lane_off + C::kColS + 128 * mt;
-                const uint32_t tO = tmem + lane_off + C::kColO + mt * D;
-                // A wait that runs out is recorded, but the loop goes on: every softmax
-                // thread must reach the named barriers below the same number of times.
-                // (After a missed phase the later parity waits return at once.)
-                if (!ttk::mbar_wait(sfull_bar(mt), (uint32_t)(j & 1))) ok = false;
-                ttk::tc_fence_after();
-                uint32_t a[32];
-                ttk::tmem_ld32(tS + k0, a);
-                ttk::tmem_ld_wait32(a);
-                if (lim < k0 + 32) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (k0 + c >= lim) a[c] = __float_as_uint(-CUDART_INF_F);
-                }
+            const int k0 = 64 * half;  // first key of this half
+            float rmax = -CUDART_INF_F;
+            {
+                uint32_t a0[32], a1[32];
+                ttk::tmem_ld32(tS + k0, a0);
+                ttk::tmem_ld32(tS + k0 + 32, a1);
+                ttk::tmem_ld_wait32(a0);
+                tie32(a1);
                 float r0 = -CUDART_INF_F, r1 = -CUDART_INF_F;
+                if (lim >= kTileKeys) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    r0 = ttk::fmax3(r0, __uint_as_float(a[c]), __uint_as_float(a[c + 1]));
-                    r1 = ttk::fmax3(r1, __uint_as_float(a[c + 2]), __uint_as_float(a[c + 3]));
-                }
-                // Row max of the raw scores over the four quarters (scale > 0 commutes),
-                // exchanged through TMEM: S columns 32q+16 .. 32q+31 hold nothing until
-                // the next QK^T (P takes the front 16), so each quarter leaves its
-                // maximum in column 32q+16 of its own lane and reads the other three.
-                ttk::tmem_st1(tS + k0 + 16, __float_as_uint(fmaxf(r0, r1)));
-                ttk::tmem_st_wait();
-                ttk::tc_fence_before();
-                named_sync(1 + mt, 512);
-                ttk::tc_fence_after();
-                uint32_t x0 = ttk::tmem_ld1(tS + 16), x1 = ttk::tmem_ld1(tS + 48);
-                uint32_t x2 = ttk::tmem_ld1(tS + 80), x3 = ttk::tmem_ld1(tS + 112);
-                ttk::tmem_ld_wait4(x0, x1, x2, x3);
-                const float mx = fmaxf(fmaxf(__uint_as_float(x0), __uint_as_float(x1)),
-                                       fmaxf(__uint_as_float(x2), __uint_as_float(x3))) * g.scale_log2;
-                if (j == 0) {
-                    m_run[mt] = mx;
+                    for (int c = 0; c < 32; c += 2) {
+                        r0 = ttk::fmax3(r0, __uint_as_float(a0[c]), __uint_as_float(a0[c + 1]));
+                        r1 = ttk::fmax3(r1, __uint_as_float(a1[c]), __uint_as_float(a1[c + 1]));
+                    }
                 } else {
-                    const bool need = mx > m_run[mt] + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, need)) {
-                        // O is stable here: PV(mt, j-1) completed before QK(mt, j).  Each
-                        // quarter rescales its D/4 columns of the row.
-                        const float alpha = need ? exp2f(m_run[mt] - mx) : 1.0f;
-                        if (need) {
-                            m_run[mt] = mx;
-                            l_part[mt] *= alpha;
-                        }
 #pragma unroll
-                        for (int cc = 0; cc < D / 4; cc += 16) {
-                            uint32_t o[16];
-                            ttk::tmem_ld16(tO + q * (D / 4) + cc, o);
-                            ttk::tmem_ld_wait16(o);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            ttk::tmem_st16(tO + q * (D / 4) + cc, o);
-                        }
+                    for (int c = 0; c < 32; ++c) {
+                        r0 = fmaxf(r0, (k0 + c < lim) ? __uint_as_float(a0[c]) : -CUDART_INF_F);
+                        r1 = fmaxf(r1, (k0 + 32 + c < lim) ? __uint_as_float(a1[c]) : -CUDART_INF_F);
                     }
                 }
-                // p = 2^(s*scale*log2e - m): one packed FMA per pair, then the SFU.  P
-                // (bf16 pairs, 16 columns) goes over the front of this quarter's own 32 S
-                // columns, which only this thread reads.  The row sum adds the same
-                // bf16-rounded p that multiply V, so the output is a weighted mean of V
-                // whose weights sum to one (a dominant key then returns its value row
-                // exactly, however p rounds).
-                const uint64_t negm2 = ttk::f2_pack(-m_run[mt], -m_run[mt]);
-                uint64_t lsum2 = ttk::f2_pack(0.f, 0.f);
+                rmax = fmaxf(r0, r1);
+            }
+            // Row max of the raw scores over both halves (scale > 0 commutes with it).
+            *my_x = rmax;
+            ttk::tc_fence_before();
+            named_sync(bar_id, 256);
+            ttk::tc_fence_after();
+            const float mx = fmaxf(*my_x, *other_x) * g.scale_log2;
+            if (j == 0) {
+                m_run = mx;
+            } else {
+                const bool need = mx > m_run + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O is stable here: PV(mt, j-1) completed before QK(mt, j).  Each
+                    // half rescales its D/2 columns of the row.
+                    const float alpha = need ? exp2f(m_run - mx) : 1.0f;
+                    if (need) {
+                        m_run = mx;
+                        l_part *= alpha;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < D / 2; cc += 32) {
+                        uint32_t o[32];
+                        ttk::tmem_ld32(tO + half * (D / 2) + cc, o);
+                        ttk::tmem_ld_wait32(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        ttk::tmem_st32(tO + half * (D / 2) + cc, o);
+                    }
+                }
+            }
+            // p = 2^(s*scale*log2e - m), 32 keys at a time re-read from TMEM: one packed
+            // FMA per pair, then the SFU.  P (bf16 pairs) goes over the front of this
+            // half's own 64 S columns, which only this thread reads.  The row sum adds
+            // the unrounded p.
+            const uint64_t negm2 = ttk::f2_pack(-m_run, -m_run);
+            uint64_t lsum2 = ttk::f2_pack(0.f, 0.f);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t a[32];
+                ttk::tmem_ld32(tS + k0 + 32 * c2, a);
+                ttk::tmem_ld_wait32(a);
+                if (lim < kTileKeys) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (k0 + 32 * c2 + c >= lim) a[c] = __float_as_uint(-CUDART_INF_F);
+                }
                 uint32_t pw[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
@@ -562,54 +451,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p0 = ttk::ex2_ftz(e0), p1 = ttk::ex2_ftz(e1);
                     const __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
                     pw[c] = *reinterpret_cast<const uint32_t*>(&pr);
-                    lsum2 = ttk::f2_add(lsum2, ttk::f2_pack(__uint_as_float(pw[c] << 16),
-                                                            __uint_as_float(pw[c] & 0xFFFF0000u)));
+                    lsum2 = ttk::f2_add(lsum2, ttk::f2_pack(p0, p1));
                 }
-                ttk::tmem_st16(tS + k0, pw);
-                {
-                    float x0, x1;
-                    ttk::f2_unpack(lsum2, x0, x1);
-                    l_part[mt] += x0 + x1;
-                }
-                if (mt == 0 && q == 0 && lim < kTileKeys) {
-                    // Last tile of a key range that ends inside it: the V rows past the end
-                    // hold whatever the cache has there.  P is 0 for them, but 0 * NaN
-                    // would still poison O, so zero those rows before PV(0, j) reads them
-                    // (PV(1, j) is issued after PV(0, j)).  K and V of this tile have
-                    // landed: QK(0, j) has completed.
-                    uint8_t* vst = smem + C::kRingV + (size_t)(j % NSV) * C::kTile;
-                    constexpr int kChunks = NP * 8;  // 16-byte chunks per V row
-                    for (int i2 = lane_row; i2 < (kTileKeys - lim) * kChunks; i2 += 128) {
-                        const int key = lim + i2 / kChunks;
-                        const int ch = i2 % kChunks;
-                        *reinterpret_cast<uint4*>(vst + (ch >> 3) * C::kPart + key * 128 + ((ch & 7) << 4)) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    ttk::fence_proxy_async_smem();
-                }
-                ttk::tmem_st_wait();
-                ttk::tc_fence_before();
-                ttk::mbar_arrive(pfull_bar(mt));
+                ttk::tmem_st16(tS + k0 + 16 * c2, pw);
             }
+            {
+                float x0, x1;
+                ttk::f2_unpack(lsum2, x0, x1);
+                l_part += x0 + x1;
+            }
+            if (q == 0 && lim < kTileKeys) {
+                // Last tile of a key range that ends inside it: the V rows past the end
+                // hold whatever the cache has there.  P is 0 for them, but 0 * NaN
+                // would still poison O, so zero those rows before PV(0, j) reads them
+                // (PV(1, j) is issued after PV(0, j)).  K and V of this tile have
+                // landed: QK(0, j) has completed.
+                uint8_t* vst = smem + C::kRing + (size_t)(j % NS) * C::kStage + C::kTile;
+                constexpr int kChunks = NP * 8;  // 16-byte chunks per V row
+                for (int i2 = lane_row; i2 < (kTileKeys - lim) * kChunks; i2 += 128) {
+                    const int key = lim + i2 / kChunks;
+                    const int ch = i2 % kChunks;
+                    *reinterpret_cast<uint4*>(vst + (ch >> 3) * C::kPart + key * 128 + ((ch & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                ttk::fence_proxy_async_smem();
+            }
+            ttk::tmem_st_wait();
+            ttk::tc_fence_before();
+            ttk::mbar_arrive(pfull_bar(mt));
         }
         if (ok) ok = ttk::mbar_wait(ofull_bar, 0);
-        // Each row's l: the sum of its four quarters' sums (same m for all of them),
-        // exchanged in the V ring, idle once every MMA has completed (o_full).
-        float l[2] = {0.f, 0.f};
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            if (mt >= n_mt) break;
-            float* xr = lx + mt * 512 + lane_row;  // [tile][quarter][row]
-            xr[128 * q] = ok ? l_part[mt] : 0.f;
-            named_sync(1 + mt, 512);
-            l[mt] = (xr[0] + xr[128]) + (xr[256] + xr[384]);
-        }
-        if (!ok && lane_row == 0 && q == 0) ttk::report_error(p.err, ttk::kErrTimeout);
+        // The row's l: this half's sum plus the other half's (same m for both).
+        float* my_l = xchg + (mt * 2 + half) * 128 + lane_row;
+        const float* other_l = xchg + (mt * 2 + (half ^ 1)) * 128 + lane_row;
+        named_sync(bar_id, 256);  // every read of the max slots is done
+        *my_l = ok ? l_part : 0.f;
+        named_sync(bar_id, 256);
+        const float l = l_part + *other_l;
+        if (!ok && lane_row == 0 && half == 0) ttk::report_error(p.err, ttk::kErrTimeout);
         // The tensor-store epilogue is chosen the same way by every thread of the CTA,
-        // and every softmax thread goes through the named barrier whether or not its
+        // and every thread of a tile goes through its named barrier whether or not its
         // waits ran out (a partial state that ran out is marked empty instead).
-        if (direct ? maps.out_tma != 0 : !g.inline_merge) {
-            // Epilogue: this quarter's D/4 columns of each O row go TMEM -> registers ->
+        if (direct ? maps.out_tma != 0 : true) {
+            // Epilogue: this half's D/2 columns of the O row go TMEM -> registers ->
             // 128-row x 128-byte boxes in shared memory (128-byte swizzle, so a warp's
             // stores of 32 rows fall in different banks; the Q tiles and the K/V ring
             // are idle once every MMA has completed) -> tensor stores issued by one
@@ -620,45 +504,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int kNbF = D / 32;  // fp32 boxes per row
             constexpr int kNbH = D / 64;  // bf16 boxes per row
             const int nb = direct ? kNbH : kNbF;
+            uint8_t* tile_base = smem + (size_t)mt * nb * 16384;
+            const float inv = 1.0f / l;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt >= n_mt) break;
-                const uint32_t tO = tmem + lane_off + C::kColO + mt * D;
-                uint8_t* tile_base = smem + (size_t)mt * nb * 16384;
-                const float inv = 1.0f / l[mt];
+            for (int cc = 0; cc < D / 2; cc += 32) {
+                uint32_t o[32];
+                ttk::tmem_ld32(tO + half * (D / 2) + cc, o);  // warp-collective: every lane loads
+                ttk::tmem_ld_wait32(o);
+                if (direct) {
 #pragma unroll
-                for (int cc = 0; cc < D / 4; cc += 16) {
-                    uint32_t o[16];
-                    ttk::tmem_ld16(tO + q * (D / 4) + cc, o);  // warp-collective: every lane loads
-                    ttk::tmem_ld_wait16(o);
-                    if (direct) {
+                    for (int e = 0; e < 4; ++e) {  // 8 bf16 = one 16-byte chunk
+                        uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {  // 8 bf16 = one 16-byte chunk
-                            uint32_t w[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const __nv_bfloat162 pr = __floats2bfloat162_rn(
-                                    __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
-                                w[u] = *reinterpret_cast<const uint32_t*>(&pr);
-                            }
-                            const int chunk = (q * (D / 4) + cc + 8 * e) / 8;
-                            uint8_t* dst = tile_base + (chunk >> 3) * 16384 + lane_row * 128 +
-                                           (((chunk & 7) ^ (lane_row & 7)) << 4);
-                            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int u = 0; u < 4; ++u) {
+                            const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                                __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
+                            w[u] = *reinterpret_cast<const uint32_t*>(&pr);
                         }
-                    } else {
+                        const int chunk = (half * (D / 2) + cc + 8 * e) / 8;
+                        uint8_t* dst = tile_base + (chunk >> 3) * 16384 + lane_row * 128 +
+                                       (((chunk & 7) ^ (lane_row & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {  // 4 fp32 = one 16-byte chunk
-                            const int chunk = (q * (D / 4) + cc + 4 * e) / 4;
-                            uint8_t* dst = tile_base + (chunk >> 3) * 16384 + lane_row * 128 +
-                                           (((chunk & 7) ^ (lane_row & 7)) << 4);
-                            *reinterpret_cast<uint4*>(dst) = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-                        }
+                    for (int e = 0; e < 8; ++e) {  // 4 fp32 = one 16-byte chunk
+                        const int chunk = (half * (D / 2) + cc + 4 * e) / 4;
+                        uint8_t* dst = tile_base + (chunk >> 3) * 16384 + lane_row * 128 +
+                                       (((chunk & 7) ^ (lane_row & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
                     }
                 }
             }
             ttk::fence_proxy_async_smem();
-            named_sync(3, 512);  // every row of every tile is staged
+            named_sync(3, 256 * n_mt);  // every row of every tile is staged
             if (q == 0 && lane_row == 0) {
                 for (int t = 0; t < n_mt; ++t) {
                     const int row0 = rg * 256 + t * 128;
@@ -674,101 +553,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ttk::bulk_commit();
                 ttk::bulk_wait_read();  // shared memory may be released; the writes land on their own
             }
-            if (q == 0) {
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    if (mt >= n_mt) break;
-                    const int r_local = mt * 128 + lane_row;
-                    const int r_glob = rg * 256 + r_local;
-                    if (r_local >= g.rows_per_cta || r_glob >= g.R) continue;
-                    if (direct) {
-                        if (p.lse != nullptr) {
-                            const int s = r_glob / g.G, jh = r_glob % g.G;
-                            p.lse[((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh] =
-                                (m_run[mt] + log2f(l[mt])) * kLn2;
-                        }
-                    } else {
-                        const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
-                        p.part_ml[2 * pi + 0] = ok ? m_run[mt] : -CUDART_INF_F;
-                        p.part_ml[2 * pi + 1] = ok ? l[mt] : 0.f;
+            if (row_valid && half == 0) {
+                if (direct) {
+                    if (p.lse != nullptr) {
+                        const int s = r_glob / g.G, jh = r_glob % g.G;
+                        p.lse[((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh] = (m_run + log2f(l)) * kLn2;
                     }
+                } else {
+                    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
+                    p.part_ml[2 * pi + 0] = ok ? m_run : -CUDART_INF_F;
+                    p.part_ml[2 * pi + 1] = ok ? l : 0.f;
                 }
             }
-        } else if (!direct) {
-            // Partial state with the combine in this kernel: this quarter's D/4 columns
-            // of each row's O and (quarter 0) its (m, l) go straight to the workspace;
-            // the last split of the row group to arrive merges every split.
-            ttk::tc_fence_after();
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt >= n_mt) break;
-                const uint32_t tO = tmem + lane_off + C::kColO + mt * D;
-                const int r_local = mt * 128 + lane_row;
-                const int r_glob = rg * 256 + r_local;
-                const bool valid = r_local < g.rows_per_cta && r_glob < g.R;
-                const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
-                float* dst = p.part_acc + pi * D + q * (D / 4);
-#pragma unroll
-                for (int cc = 0; cc < D / 4; cc += 16) {
-                    uint32_t o[16];
-                    ttk::tmem_ld16(tO + q * (D / 4) + cc, o);  // warp-collective: every lane loads
-                    ttk::tmem_ld_wait16(o);
-                    if (valid) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            __stcg(reinterpret_cast<float4*>(dst + cc) + e,
-                                   make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                               __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3])));
-                    }
-                }
-                if (valid && q == 0) {
-                    __stcg(p.part_ml + 2 * pi + 0, ok ? m_run[mt] : -CUDART_INF_F);
-                    __stcg(p.part_ml + 2 * pi + 1, ok ? l[mt] : 0.f);
-                }
-            }
-            arrive_and_merge<D>(p, item, b, gkv, rg, nv, tid - 128, 512, flag_slot, 3);
         } else if (ok) {
             // Single split with G not dividing 128 (no box covers whole positions):
-            // each quarter row goes TMEM -> registers -> shared memory -> one bulk copy.
-            // A slot stride of D/2 + 16 bytes keeps the 16-byte stores of consecutive
+            // each half row goes TMEM -> registers -> shared memory -> one bulk copy.
+            // A row stride of D*2 + 16 bytes keeps the 16-byte stores of consecutive
             // rows in different banks.
             ttk::tc_fence_after();
+            uint8_t* hrow = smem + (size_t)(r_local * 2 + half) * C::kHalfRow;
+            const float inv = 1.0f / l;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt >= n_mt) break;
-                const uint32_t tO = tmem + lane_off + C::kColO + mt * D;
-                const int r_local = mt * 128 + lane_row;
-                const int r_glob = rg * 256 + r_local;
-                const bool valid = r_local < g.rows_per_cta && r_glob < g.R;
-                uint8_t* qrow_s = smem + (size_t)(r_local * 4 + q) * C::kQuarterRow;
-                const float inv = 1.0f / l[mt];
+            for (int cc = 0; cc < D / 2; cc += 32) {
+                uint32_t o[32];
+                ttk::tmem_ld32(tO + half * (D / 2) + cc, o);  // warp-collective: every lane loads
+                ttk::tmem_ld_wait32(o);
 #pragma unroll
-                for (int cc = 0; cc < D / 4; cc += 16) {
-                    uint32_t o[16];
-                    ttk::tmem_ld16(tO + q * (D / 4) + cc, o);  // warp-collective: every lane loads
-                    ttk::tmem_ld_wait16(o);
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const __nv_bfloat162 pr = __floats2bfloat162_rn(
-                                __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
-                            w[u] = *reinterpret_cast<const uint32_t*>(&pr);
-                        }
-                        *reinterpret_cast<uint4*>(qrow_s + (cc + 8 * e) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int u = 0; u < 4; ++u) {
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                            __uint_as_float(o[8 * e + 2 * u]) * inv, __uint_as_float(o[8 * e + 2 * u + 1]) * inv);
+                        w[u] = *reinterpret_cast<const uint32_t*>(&pr);
                     }
-                }
-                if (valid) {
-                    ttk::fence_proxy_async_smem();
-                    const int s = r_glob / g.G, jh = r_glob % g.G;
-                    const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh;
-                    ttk::bulk_store(p.out + orow * D + q * (D / 4), ttk::smem_u32(qrow_s), D / 2);
-                    ttk::bulk_commit();
-                    if (q == 0 && p.lse != nullptr) p.lse[orow] = (m_run[mt] + log2f(l[mt])) * kLn2;
+                    *reinterpret_cast<uint4*>(hrow + (cc + 8 * e) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            ttk::bulk_wait_read();  // shared memory may be released; the writes land on their own
+            if (row_valid) {
+                ttk::fence_proxy_async_smem();
+                const int s = r_glob / g.G, jh = r_glob % g.G;
+                const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + jh;
+                ttk::bulk_store(p.out + orow * D + half * (D / 2), ttk::smem_u32(hrow), D);
+                ttk::bulk_commit();
+                if (half == 0 && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
+                ttk::bulk_wait_read();  // shared memory may be released; the writes land on their own
+            }
         }
     }
 
@@ -875,12 +705,7 @@ long long split_cost(long long items, int n_tiles, int splits) {
     const long long ctas = items * splits;
     const long long waves = (ctas + 147) / 148;
     const long long tps = (n_tiles + splits - 1) / splits;
-    long long merge = 0;  // one split: no combine at all
-    if (splits > 1 && splits <= kAttnInlineMergeMax)
-        merge = 3;        // the last split CTA merges at most four partial states
-    else if (splits > 1)
-        merge = 4 + 4 * ((splits + 7) / 8) + (2 * ctas) / 148;  // a second launch
-    return 4 * waves * (tps + 3) + merge;
+    return 4 * waves * (tps + 3) + 4 * ((splits + 7) / 8) + (2 * ctas) / 148;
 }
 
 }  // namespace
@@ -942,12 +767,12 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     g.n_splits = n_tiles > 0 ? (n_tiles + tps - 1) / tps : 1;
     if (g.n_splits > 65535) { *why = "too many context splits"; return false; }
     if ((long long)B * Hkv * g.n_rg > 0x7fffffffLL) { *why = "too many row groups"; return false; }
-    g.inline_merge = (g.n_splits > 1 && g.n_splits <= kAttnInlineMergeMax) ? 1 : 0;
+    g.inline_merge = 0;
     return true;
 }
 
 // Workspace: fp32 partial accumulators [B][Hkv][n_splits][R][D], then (m, l) pairs,
-// then one ticket per row group [B][Hkv][n_rg] (zero on entry, left at zero).
+// then one counter word per row group [B][Hkv][n_rg] (zero on entry, left at zero).
 void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
