@@ -614,14 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------------
 // Combine: partial states of the context splits -> out, lse.  One warp per output
-// row (b, s, h); lanes hold D/32 columns each.
+// row (b, s, h); lanes hold D/32 columns each.  Every split's (m, l) pair and the
+// lane's accumulator slice are requested together, eight splits per round trip (the
+// pass is latency-bound: a few hundred bytes per row), and folded into a running
+// (max, sum, accumulator) as they arrive.
 // ---------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
     ttk::pdl_wait();
     ttk::pdl_trigger();
     constexpr int PER = D / 32;
-    constexpr int kBatch = 8;  // accumulators requested together
+    constexpr int kBatch = 8;  // splits requested together
     const AttnGeom& g = p.g;
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -639,53 +642,52 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
     const int n_valid = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
     const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + (size_t)(s * g.G + j);
 
-    float m = -CUDART_INF_F;
-    for (int c = lane; c < n_valid; c += 32) m = fmaxf(m, __ldcg(p.part_ml + 2 * (base + (size_t)c * g.R)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float m = -CUDART_INF_F, lsum = 0.f;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float lsum = 0.f;
-    for (int c0 = 0; c0 < n_valid; c0 += 32) {
-        // lane c - c0 holds split c's weight; an empty partial state (m = -inf) gets
-        // weight 0 and is selected away, since its accumulator was never written.
-        const int c = c0 + lane;
-        float wc = 0.f;
-        if (c < n_valid) {
-            const size_t pi = base + (size_t)c * g.R;
-            const float mc = __ldcg(p.part_ml + 2 * pi);
-            if (mc != -CUDART_INF_F) {
-                wc = exp2f(mc - m);
-                lsum = fmaf(wc, __ldcg(p.part_ml + 2 * pi + 1), lsum);
+    for (int c0 = 0; c0 < n_valid; c0 += kBatch) {
+        const int nc = min(kBatch, n_valid - c0);
+        float mc[kBatch], lc[kBatch], a[kBatch][PER];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int cu = c0 + min(u, nc - 1);  // in range; repeats beyond nc are not used
+            const size_t pi = base + (size_t)cu * g.R;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pi);
+            mc[u] = ml.x;
+            lc[u] = ml.y;
+            const float* ap = p.part_acc + pi * D + lane * PER;
+            if (PER == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(ap));
+                a[u][0] = v.x; a[u][1 % PER] = v.y; a[u][2 % PER] = v.z; a[u][3 % PER] = v.w;
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(ap));
+                a[u][0] = v.x; a[u][1 % PER] = v.y;
             }
         }
-        const int nc = min(32, n_valid - c0);
-        for (int cb = 0; cb < nc; cb += kBatch) {
-            float a[kBatch][PER];
+        // an empty partial state (m = -inf) carries no weight; its accumulator was
+        // never written and is not used
+        float mn = m;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int cu = min(cb + u, nc - 1);  // in range; duplicates get weight 0 below
-                const float* ap = p.part_acc + (base + (size_t)(c0 + cu) * g.R) * D + lane * PER;
-                if (PER == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(ap));
-                    a[u][0] = v.x; a[u][1 % PER] = v.y; a[u][2 % PER] = v.z; a[u][3 % PER] = v.w;
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2*>(ap));
-                    a[u][0] = v.x; a[u][1 % PER] = v.y;
-                }
-            }
+        for (int u = 0; u < kBatch; ++u)
+            if (u < nc) mn = fmaxf(mn, mc[u]);
+        if (mn == -CUDART_INF_F) continue;
+        if (m != -CUDART_INF_F && mn != m) {
+            const float r = exp2f(m - mn);
+            lsum *= r;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                float w = __shfl_sync(0xffffffffu, wc, min(cb + u, 31));
-                if (cb + u >= nc) w = 0.f;
+            for (int e = 0; e < PER; ++e) acc[e] *= r;
+        }
+        m = mn;
 #pragma unroll
-                for (int e = 0; e < PER; ++e) acc[e] = (w != 0.f) ? fmaf(w, a[u][e], acc[e]) : acc[e];
-            }
+        for (int u = 0; u < kBatch; ++u) {
+            if (u >= nc || mc[u] == -CUDART_INF_F) continue;
+            const float w = exp2f(mc[u] - m);
+            lsum = fmaf(w, lc[u], lsum);
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, a[u][e], acc[e]);
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     const float inv = 1.0f / lsum;
     const size_t orow = ((size_t)b * g.S + s) * g.Hq + h;
     uint16_t* op = p.out + orow * D + lane * PER;
