@@ -116,13 +116,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const AttnGeom& g = p.g;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    // Grid: x = row group item (rg fastest, then kv head, then sequence), y = split.
-    // Splits vary slowest, so on a ragged batch the short last splits of long
-    // sequences are dispatched last and the tail of the grid is short.
-    const int rg = blockIdx.x % g.n_rg;
-    const int gkv = (blockIdx.x / g.n_rg) % g.Hkv;
-    const int b = blockIdx.x / (g.n_rg * g.Hkv);
-    const int split = blockIdx.y;
+    // Work unit u = item + n_items * split, item = rg + n_rg * (kv head + Hkv * sequence).
+    // Grid: x = item, y = split, so splits vary slowest; on a ragged batch (lpt) a 1-D
+    // grid takes the units longest first from the order the prep kernel sorted, and the
+    // CTAs past the non-empty units exit.
+    const int n_items = g.B * g.Hkv * g.n_rg;
+    long long unit = (long long)blockIdx.y * n_items + blockIdx.x;
+    if (p.order != nullptr) {
+        const long long n_units = (long long)n_items * g.n_splits;
+        if ((long long)blockIdx.x >= __ldg(p.order + n_units)) return;
+        unit = __ldg(p.order + blockIdx.x);
+    }
+    const int item = (int)(unit % n_items);
+    const int rg = item % g.n_rg;
+    const int gkv = (item / g.n_rg) % g.Hkv;
+    const int b = item / (g.n_rg * g.Hkv);
+    const int split = (int)(unit / n_items);
 
     if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return;
     const int cap = g.page_size ? g.max_pages * g.page_size : g.max_ctx;
@@ -615,16 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------
 // Combine: partial states of the context splits -> out, lse.  One warp per output
 // row (b, s, h); lanes hold D/32 columns each.  Every split's (m, l) pair and the
-// lane's accumulator slice are requested together, eight splits per round trip (the
-// pass is latency-bound: a few hundred bytes per row), and folded into a running
-// (max, sum, accumulator) as they arrive.
+// lane's accumulator slice are requested together, four or eight splits per round
+// trip (the pass is latency-bound: a few hundred bytes per row, so with at most four
+// splits the smaller batch's registers leave room for more rows in flight per SM),
+// and folded into a running (max, sum, accumulator) as they arrive.
 // ---------------------------------------------------------------------------------
-template <int D>
+template <int D, int kBatch>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
     ttk::pdl_wait();
     ttk::pdl_trigger();
-    constexpr int PER = D / 32;
-    constexpr int kBatch = 8;  // splits requested together
+    constexpr int PER = D / 32;  // kBatch: splits requested together (4 or 8)
     const AttnGeom& g = p.g;
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -699,6 +708,55 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
     if (p.lse != nullptr && lane == 0) p.lse[orow] = (m + log2f(lsum)) * kLn2;
 }
 
+// Work units of a ragged batch sorted by their number of key tiles, longest first (a
+// counting sort in one CTA; the hardware then dispatches the long units first and the
+// grid's tail is short).  A unit's length is the split's context tiles plus the
+// block's own keys on split 0; sequences that are skipped or finished have none.
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_constant__ AttnSplitParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
+    __shared__ int hist[kOrderMaxLen + 1];
+    const AttnGeom& g = p.g;
+    const int n_items = g.B * g.Hkv * g.n_rg;
+    const int n_units = n_items * g.n_splits;
+    const int cap = g.page_size ? g.max_pages * g.page_size : g.max_ctx;
+    int32_t* order = const_cast<int32_t*>(p.order);
+    auto unit_len = [&](int u) -> int {
+        const int item = u % n_items, split = u / n_items;
+        const int b = item / (g.n_rg * g.Hkv);
+        if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return 0;
+        const int ctx = p.ctx_len ? __ldg(p.ctx_len + b) : g.max_ctx;
+        if (ctx < 0 || ctx > cap) return split == 0 ? 1 : 0;  // the split pass reports it
+        const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
+        const int t0 = split * g.tiles_per_split;
+        const int t1 = min(n_tiles, t0 + g.tiles_per_split);
+        return (split == 0 ? 1 : 0) + max(0, t1 - t0);
+    };
+    for (int i = threadIdx.x; i <= kOrderMaxLen; i += kOrderThreads) hist[i] = 0;
+    __syncthreads();
+    for (int u = threadIdx.x; u < n_units; u += kOrderThreads) {
+        const int len = unit_len(u);
+        if (len > 0) atomicAdd(&hist[min(len, kOrderMaxLen)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // start of each length's slots, longest first
+        int run = 0;
+        for (int len = kOrderMaxLen; len >= 1; --len) {
+            const int c = hist[len];
+            hist[len] = run;
+            run += c;
+        }
+        order[n_units] = run;
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < n_units; u += kOrderThreads) {
+        const int len = unit_len(u);
+        if (len > 0) order[atomicAdd(&hist[min(len, kOrderMaxLen)], 1)] = u;
+    }
+}
+
 // Modelled cost, in quarter tile-times, of splitting every (sequence, kv head, row
 // group) item's n_tiles context tiles into `splits` ranges: waves of one CTA per SM,
 // each paying its tiles plus ~3 tiles of set-up, pipeline fill and epilogue; the merge's
@@ -768,28 +826,37 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     g.tiles_per_split = tps;
     g.n_splits = n_tiles > 0 ? (n_tiles + tps - 1) / tps : 1;
     if (g.n_splits > 65535) { *why = "too many context splits"; return false; }
-    if ((long long)B * Hkv * g.n_rg > 0x7fffffffLL) { *why = "too many row groups"; return false; }
+    if ((long long)B * Hkv * g.n_rg * g.n_splits > 0x7fffffffLL) { *why = "too many work units"; return false; }
     g.inline_merge = 0;
+    // Ragged batches spanning several waves: units dispatched longest first.  The sort
+    // is a counting sort over lengths of at most tiles_per_split + 1 tiles.
+    g.lpt = (page_size != 0 && (long long)B * Hkv * g.n_rg * g.n_splits > 148 && tps + 1 <= kOrderMaxLen &&
+             (long long)B * Hkv * g.n_rg * g.n_splits <= kOrderMaxUnits) ? 1 : 0;
     return true;
 }
 
 // Workspace: fp32 partial accumulators [B][Hkv][n_splits][R][D], then (m, l) pairs,
 // then one counter word per row group [B][Hkv][n_rg] (zero on entry, left at zero).
-void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket) {
+void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket,
+                 int32_t** order) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
+    size_t tk = ((size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
     char* w = static_cast<char*>(ws);
     *part_acc = reinterpret_cast<float*>(w);
     *part_ml = reinterpret_cast<float*>(w + acc);
     *ticket = reinterpret_cast<unsigned*>(w + acc + ml);
+    *order = g.lpt ? reinterpret_cast<int32_t*>(w + acc + ml + tk) : nullptr;
 }
 
 size_t attn_workspace_bytes(const AttnGeom& g) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
-    return acc + ml + (size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 256;
+    size_t tk = ((size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
+    const size_t units = (size_t)g.B * g.Hkv * g.n_rg * g.n_splits;
+    return acc + ml + tk + (g.lpt ? (units + 1) * sizeof(int32_t) : 0) + 256;
 }
 
 cudaError_t attn_split_prepare(int D) {
@@ -809,9 +876,14 @@ cudaError_t attn_split_prepare(int D) {
     return e;
 }
 
+cudaError_t launch_attn_order(const AttnSplitParams& p, cudaStream_t stream) {
+    return launch_pdl(attn_order_kernel, dim3(1), dim3(kOrderThreads), 0, stream, p);
+}
+
 cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cudaStream_t stream) {
     const AttnGeom& g = p.g;
-    dim3 grid((unsigned)(g.B * g.Hkv * g.n_rg), (unsigned)g.n_splits, 1);
+    const unsigned n_items = (unsigned)(g.B * g.Hkv * g.n_rg);
+    dim3 grid = p.order ? dim3(n_items * (unsigned)g.n_splits, 1, 1) : dim3(n_items, (unsigned)g.n_splits, 1);
     if (g.D == 128)
         return launch_pdl(attn_split_kernel<128>, grid, dim3(kThreads), Cfg<128>::kBytes, stream, p, maps);
     else
@@ -823,10 +895,13 @@ cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream) {
     const long long rows = (long long)g.B * g.S * g.Hq;
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const bool few = g.n_splits <= 4;
     if (g.D == 128)
-        return launch_pdl(attn_merge_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
+        return few ? launch_pdl(attn_merge_kernel<128, 4>, dim3((unsigned)blocks), dim3(256), 0, stream, p)
+                   : launch_pdl(attn_merge_kernel<128, 8>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
     else
-        return launch_pdl(attn_merge_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
+        return few ? launch_pdl(attn_merge_kernel<64, 4>, dim3((unsigned)blocks), dim3(256), 0, stream, p)
+                   : launch_pdl(attn_merge_kernel<64, 8>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
 }
 
 }  // namespace tti

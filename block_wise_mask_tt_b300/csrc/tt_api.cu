@@ -206,7 +206,9 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     float* part_acc = nullptr;
     float* part_ml = nullptr;
     unsigned* ticket = nullptr;
-    tti::attn_layout(g, ws, &part_acc, &part_ml, &ticket);
+    int32_t* order = nullptr;
+    if (!pl.has_ctx) g.lpt = 0;
+    tti::attn_layout(g, ws, &part_acc, &part_ml, &ticket, &order);
     // Epilogue store maps: partial states when the context is split and a second pass
     // combines them; the output itself wherever a CTA may write it directly (when G
     // divides 128, so that a 128-row tile covers whole positions).
@@ -237,9 +239,11 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     sp.part_acc = part_acc;
     sp.part_ml = part_ml;
     sp.ticket = ticket;
+    sp.order = order;
     sp.out = static_cast<uint16_t*>(out);
     sp.lse = lse;
     sp.err = err;
+    if (order != nullptr) TT_CUDA(tti::launch_attn_order(sp, st));
     TT_CUDA(tti::launch_attn_split(sp, maps, st));
     if (g.n_splits > 1 && !g.inline_merge) {
         tti::AttnMergeParams mp;

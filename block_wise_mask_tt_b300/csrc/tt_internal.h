@@ -152,15 +152,20 @@ struct AttnGeom {
     int n_splits;
     int tiles_per_split;  // 128-token tiles per split
     int inline_merge;     // 1: the last split CTA of a row group merges (n_splits <= 4)
+    int lpt;              // 1: work units dispatched longest first (ragged paged batches)
     float scale_log2;     // softmax_scale * log2(e)
 };
 constexpr int kAttnInlineMergeMax = 4;  // most splits the split kernel merges itself
+constexpr int kOrderMaxLen = 1024;       // longest unit (tiles) the longest-first order sorts
+constexpr int kOrderMaxUnits = 1 << 20;  // most work units it sorts
 bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_size,
                    int max_pages, int num_pages, float softmax_scale, int num_splits,
                    AttnGeom& g, const char** why);
 size_t attn_workspace_bytes(const AttnGeom& g);
-// Pointers into a workspace of attn_workspace_bytes(g) bytes.
-void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket);
+// Pointers into a workspace of attn_workspace_bytes(g) bytes.  order (lpt only):
+// the work units sorted by length, then their count.
+void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket,
+                 int32_t** order);
 
 struct AttnSplitParams {
     AttnGeom g;
@@ -171,6 +176,7 @@ struct AttnSplitParams {
     float* part_acc;             // [B][Hkv][n_splits][R][D]
     float* part_ml;              // [B][Hkv][n_splits][R][2]
     unsigned int* ticket;        // [B][Hkv][n_rg]: zero on entry and on exit (inline merge)
+    const int32_t* order;        // lpt: [units] work unit of each CTA, then the count
     uint16_t* out;               // bf16 [B][S][Hq][D]: written here when n_splits == 1 or
                                  // when the split kernel merges (inline_merge)
     float* lse;                  // nullable, [B][S][Hq]: likewise
@@ -189,6 +195,9 @@ struct AttnMaps {
     int out_tma;
 };
 cudaError_t attn_split_prepare(int D);  // sets the kernel's shared-memory limit on this device
+// lpt: sorts the non-empty (row group, split) work units by their number of key tiles,
+// longest first, into p.order (one CTA, before the split pass).
+cudaError_t launch_attn_order(const AttnSplitParams& p, cudaStream_t stream);
 cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cudaStream_t stream);
 
 struct AttnMergeParams {

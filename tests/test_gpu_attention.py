@@ -93,6 +93,18 @@ def test_split_invariance(tt, splits):
     check_attention(O, Or, lse, lr, what=f"splits={splits}")
 
 
+@pytest.mark.parametrize("splits", [0, 3, 7])
+def test_ragged_paged_longest_first(tt, splits):
+    """A ragged paged batch of more work units than SMs: the units are dispatched
+    longest first from a device-side sort (empty splits of short sequences left out);
+    with 7 splits the combine pass merges them, with 3 the split CTAs' partials too."""
+    w = W(B=40, L=700, L_min=1, S=16, Hq=8, Hkv=2, D=64, paged=True, softmax_scale=0.125)
+    inp = synth.make_attention_inputs(w, seed=15)
+    O, lse = run_attn(tt, w, inp, num_splits=splits)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr, what=f"splits={splits}")
+
+
 def test_paged_equals_contiguous(tt):
     w = W(B=3, L=500, L_min=1, S=16, Hq=32, Hkv=2, D=128, paged=True, q_prescale=1 / math.sqrt(128))
     inp = synth.make_attention_inputs(w, seed=12)
