@@ -149,7 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = nblk + max(0, t1 - t0);
     if (nt == 0) return;  // this split is empty; the combine pass does not read it
     const int n_mt = g.n_mt;
-    const bool direct = g.n_splits == 1;
+    // Direct: this CTA sees every key of its rows (its row group has one non-empty
+    // split) and writes the normalised output itself; the combine pass skips the rows.
+    const int nv = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
+    const bool direct = g.n_splits == 1 || nv == 1;
 
     if (g.page_size && t1 > t0) {
         // Every page this split reads must exist; pages past the context end are not read.
@@ -647,8 +650,10 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
     int ctx = p.ctx_len ? __ldg(p.ctx_len + b) : g.max_ctx;
     if (ctx < 0 || ctx > cap) ctx = 0;  // reported by the split pass
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
-    // Split 0 always holds the block's keys; the others hold context tiles.
+    // Split 0 always holds the block's keys; the others hold context tiles.  A row group
+    // with one non-empty split was written by the split pass directly.
     const int n_valid = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
+    if (n_valid == 1) return;
     const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + (size_t)(s * g.G + j);
 
     float m = -CUDART_INF_F, lsum = 0.f;
@@ -818,9 +823,27 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
             if (c < best_cost) { best_cost = c; best = s; }
         }
         tps = (n_tiles + best - 1) / best;
-        // A paged batch is ragged: shorter sequences leave their later splits empty
-        // (those CTAs exit at once), so keep splits long enough to amortise a CTA.
-        if (page_size != 0 && tps < 64 && n_tiles > 64) tps = 64;
+        if (page_size != 0 && items > 148) {
+            // A ragged paged batch of several waves is dispatched longest unit first, so
+            // its span is about max(longest unit, total tiles / SMs) plus per-CTA fill
+            // and the combine.  With lengths taken as uniform up to max_ctx: when the
+            // longest possible unit is within a quarter of the per-SM share, one split
+            // (no partial states, no combine) is best; otherwise units are cut at the
+            // share (at least 64 tiles), so only the longest sequences are split.
+            const long long total = items * (long long)(n_tiles + 1) / 2;
+            const long long share = (total + 147) / 148;
+            if (n_tiles + 1 <= share + share / 4) {
+                tps = n_tiles;
+            } else {
+                tps = (int)share;
+                if (tps < 64) tps = 64;
+                if (tps > n_tiles) tps = n_tiles;
+            }
+        } else if (page_size != 0 && tps < 64 && n_tiles > 64) {
+            // shorter sequences of a paged batch leave their later splits empty (those
+            // CTAs exit at once), so keep splits long enough to amortise a CTA
+            tps = 64;
+        }
     }
     if (tps < 1) tps = 1;
     g.tiles_per_split = tps;

@@ -222,7 +222,8 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
         const cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)g.R * g.D * 4};
         const cuuint32_t box[3] = {32, 128, 1};
         TT_TRY(encode_map(&maps.part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part_acc, dims, strides, box));
-    } else if (128 % g.G == 0) {
+    }
+    if (128 % g.G == 0) {
         const cuuint64_t dims[4] = {(cuuint64_t)g.D, (cuuint64_t)g.Hq, (cuuint64_t)g.S, (cuuint64_t)g.B};
         const cuuint64_t strides[3] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.Hq * g.D * 2,
                                        (cuuint64_t)g.S * g.Hq * g.D * 2};
