@@ -122,10 +122,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // CTAs past the non-empty units exit.
     const int n_items = g.B * g.Hkv * g.n_rg;
     long long unit = (long long)blockIdx.y * n_items + blockIdx.x;
+    int tps = g.tiles_per_split;
     if (p.order != nullptr) {
         const long long n_units = (long long)n_items * g.n_splits;
         if ((long long)blockIdx.x >= __ldg(p.order + n_units)) return;
         unit = __ldg(p.order + blockIdx.x);
+        tps = __ldg(p.order + n_units + 1);  // this call's split length
     }
     const int item = (int)(unit % n_items);
     const int rg = item % g.n_rg;
@@ -143,15 +145,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Tiles of this CTA: split 0 starts with the block's own keys, then context tiles
     // t0 .. t1-1.
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
-    const int t0 = split * g.tiles_per_split;
-    const int t1 = min(n_tiles, t0 + g.tiles_per_split);
+    const int t0 = split * tps;
+    const int t1 = min(n_tiles, t0 + tps);
     const int nblk = (split == 0) ? 1 : 0;
     const int nt = nblk + max(0, t1 - t0);
     if (nt == 0) return;  // this split is empty; the combine pass does not read it
     const int n_mt = g.n_mt;
     // Direct: this CTA sees every key of its rows (its row group has one non-empty
     // split) and writes the normalised output itself; the combine pass skips the rows.
-    const int nv = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
+    const int nv = max(1, (n_tiles + tps - 1) / tps);
     const bool direct = g.n_splits == 1 || nv == 1;
 
     if (g.page_size && t1 > t0) {
@@ -377,13 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bar_id = 1 + mt;  // named barrier of this tile's two halves
         float m_run = -CUDART_INF_F;
         float l_part = 0.f;  // sum of p over this half's keys
+        // keys of round j at or past lim lie outside: S on the block's round, else the
+        // context end less the round's first key
+        const int lim_ctx = ctx - (t0 - nblk) * kTileKeys;
         for (int j = 0; j < nt; ++j) {
             // A wait that runs out is recorded, but the loop goes on: every thread of
             // the tile must reach the named barriers below the same number of times.
             // (After a missed phase the later parity waits return at once.)
             if (!ttk::mbar_wait(sfull_bar(mt), (uint32_t)(j & 1))) ok = false;
             ttk::tc_fence_after();
-            const int lim = (j < nblk) ? g.S : ctx - (t0 + j - nblk) * kTileKeys;  // keys >= lim lie outside
+            const int lim = (j < nblk) ? g.S : lim_ctx - j * kTileKeys;
             const int k0 = 64 * half;  // first key of this half
             float rmax = -CUDART_INF_F;
             {
@@ -630,17 +635,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // lane's accumulator slice are requested together, four or eight splits per round
 // trip (the pass is latency-bound: a few hundred bytes per row, so with at most four
 // splits the smaller batch's registers leave room for more rows in flight per SM),
-// and folded into a running (max, sum, accumulator) as they arrive.
+// and folded into a running (max, sum, accumulator) as they arrive.  When the prep
+// kernel chose the split length, the grid is one resident wave striding over the rows:
+// most calls then have few or no split row groups, and the wave exits at once.
 // ---------------------------------------------------------------------------------
 template <int D, int kBatch>
-__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
-    ttk::pdl_wait();
-    ttk::pdl_trigger();
+__device__ __forceinline__ void merge_row(const AttnMergeParams& p, long long row, int tps) {
     constexpr int PER = D / 32;  // kBatch: splits requested together (4 or 8)
     const AttnGeom& g = p.g;
     const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= (long long)g.B * g.S * g.Hq) return;
     const int h = (int)(row % g.Hq);
     const int s = (int)((row / g.Hq) % g.S);
     const int b = (int)(row / ((long long)g.Hq * g.S));
@@ -652,7 +655,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
     const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
     // Split 0 always holds the block's keys; the others hold context tiles.  A row group
     // with one non-empty split was written by the split pass directly.
-    const int n_valid = max(1, (n_tiles + g.tiles_per_split - 1) / g.tiles_per_split);
+    const int n_valid = max(1, (n_tiles + tps - 1) / tps);
     if (n_valid == 1) return;
     const size_t base = ((size_t)(b * g.Hkv + gkv) * g.n_splits) * (size_t)g.R + (size_t)(s * g.G + j);
 
@@ -713,47 +716,166 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
     if (p.lse != nullptr && lane == 0) p.lse[orow] = (m + log2f(lsum)) * kLn2;
 }
 
-// Work units of a ragged batch sorted by their number of key tiles, longest first (a
+template <int D, int kBatch>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnMergeParams p) {
+    ttk::pdl_wait();
+    ttk::pdl_trigger();
+    const AttnGeom& g = p.g;
+    int tps = g.tiles_per_split;
+    if (p.order != nullptr) {
+        const long long n_units = (long long)g.B * g.Hkv * g.n_rg * g.n_splits;
+        if (__ldg(p.order + n_units + 2) == 0) return;  // this call split no row group
+        tps = __ldg(p.order + n_units + 1);
+    }
+    const long long rows = (long long)g.B * g.S * g.Hq;
+    const long long stride = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += stride)
+        merge_row<D, kBatch>(p, row, tps);
+}
+
+// Work units of a ragged batch, sorted by their number of key tiles, longest first (a
 // counting sort in one CTA; the hardware then dispatches the long units first and the
 // grid's tail is short).  A unit's length is the split's context tiles plus the
 // block's own keys on split 0; sequences that are skipped or finished have none.
+// With lpt_dyn the split length is chosen here, per call, from the active sequences:
+// tiles_per_split times 1, 2, 4, ... (at most the longest context), by an estimate of
+// the span in tile-times: max(longest unit, total / SMs) + ~4 tiles of pipeline fill
+// per wave of CTAs + ~32 tiles when anything is split (partial states and the combine
+// pass; fitted to the ragged paged batch: one split 459 us, units of the per-SM share
+// 466 us, two splits 497 us).  A block's first step (every sequence active) then takes
+// whole row groups and no combine; later steps, with a few long sequences left, cut
+// them into 64-tile units.
+// Output: order[0 .. count) units, order[n_units] = count, order[n_units + 1] = split
+// length, order[n_units + 2] = 1 if some row group has more than one split.
 constexpr int kOrderThreads = 1024;
+constexpr int kOrderCands = 8;  // split lengths tried: tiles_per_split << 0 .. 7
 __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_constant__ AttnSplitParams p) {
     ttk::pdl_wait();
     ttk::pdl_trigger();
     __shared__ int hist[kOrderMaxLen + 1];
+    __shared__ unsigned s_total, s_lmax, s_active, s_units[kOrderCands];
+    __shared__ int s_tps, s_split;
     const AttnGeom& g = p.g;
     const int n_items = g.B * g.Hkv * g.n_rg;
     const int n_units = n_items * g.n_splits;
     const int cap = g.page_size ? g.max_pages * g.page_size : g.max_ctx;
+    const int base = g.tiles_per_split;
     int32_t* order = const_cast<int32_t*>(p.order);
-    auto unit_len = [&](int u) -> int {
-        const int item = u % n_items, split = u / n_items;
+    // context tiles of an item's sequence, or -1 when it takes no part in this call
+    auto item_tiles = [&](int item) -> int {
         const int b = item / (g.n_rg * g.Hkv);
-        if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return 0;
+        if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return -1;
         const int ctx = p.ctx_len ? __ldg(p.ctx_len + b) : g.max_ctx;
-        if (ctx < 0 || ctx > cap) return split == 0 ? 1 : 0;  // the split pass reports it
-        const int n_tiles = (ctx + kTileKeys - 1) / kTileKeys;
-        const int t0 = split * g.tiles_per_split;
-        const int t1 = min(n_tiles, t0 + g.tiles_per_split);
-        return (split == 0 ? 1 : 0) + max(0, t1 - t0);
+        if (ctx < 0 || ctx > cap) return 0;  // split 0 alone: the split pass reports it
+        return (ctx + kTileKeys - 1) / kTileKeys;
     };
     for (int i = threadIdx.x; i <= kOrderMaxLen; i += kOrderThreads) hist[i] = 0;
+    if (threadIdx.x == 0) {
+        s_total = 0;
+        s_lmax = 0;
+        s_active = 0;
+        for (int c = 0; c < kOrderCands; ++c) s_units[c] = 0;
+    }
     __syncthreads();
+    if (g.lpt_dyn) {
+        // Sums over the items (each below 2^31: at most kOrderMaxUnits items of at most
+        // kOrderMaxLen tiles), reduced per warp, one shared atomic per warp and sum.
+        unsigned tot = 0, lmax = 0, active = 0, units[kOrderCands] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int it = threadIdx.x; it < n_items; it += kOrderThreads) {
+            const int L = item_tiles(it);
+            if (L < 0) continue;
+            ++active;
+            tot += (unsigned)L + 1u;
+            lmax = max(lmax, (unsigned)L);
+#pragma unroll
+            for (int c = 0; c < kOrderCands; ++c) units[c] += (unsigned)max(1, (L + (base << c) - 1) / (base << c));
+        }
+        tot = __reduce_add_sync(0xffffffffu, tot);
+        lmax = __reduce_max_sync(0xffffffffu, lmax);
+        active = __reduce_add_sync(0xffffffffu, active);
+#pragma unroll
+        for (int c = 0; c < kOrderCands; ++c) units[c] = __reduce_add_sync(0xffffffffu, units[c]);
+        if ((threadIdx.x & 31) == 0) {
+            atomicAdd(&s_total, tot);
+            atomicMax(&s_lmax, lmax);
+            atomicAdd(&s_active, active);
+#pragma unroll
+            for (int c = 0; c < kOrderCands; ++c) atomicAdd(&s_units[c], units[c]);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const long long n_active = (long long)s_active;
+            const long long share = ((long long)s_total + 147) / 148;
+            long long best = -1;
+            int best_c = 0;
+            for (int c = 0; c < kOrderCands; ++c) {
+                const long long t = (long long)base << c;
+                if (c > 0 && ((long long)base << (c - 1)) >= s_lmax) break;  // longer splits change nothing
+                const long long longest = (t < (long long)s_lmax ? t : (long long)s_lmax) + 1;
+                const long long waves = ((long long)s_units[c] + 147) / 148;
+                const bool split = (long long)s_units[c] > n_active;
+                const long long est = max(longest, share) + 4 * waves + (split ? 32 : 0);
+                if (best < 0 || est <= best) {
+                    best = est;
+                    best_c = c;
+                }
+            }
+            s_tps = base << best_c;
+            s_split = (long long)s_units[best_c] > n_active ? 1 : 0;
+        }
+    } else if (threadIdx.x == 0) {
+        s_tps = base;
+        s_split = g.n_splits > 1 ? 1 : 0;
+    }
+    __syncthreads();
+    const int tps = s_tps;
+    auto unit_len = [&](int u) -> int {
+        const int item = u % n_items, split = u / n_items;
+        const int L = item_tiles(item);
+        if (L < 0) return 0;
+        const int t0 = split * tps;
+        const int t1 = min(L, t0 + tps);
+        return (split == 0 ? 1 : 0) + max(0, t1 - t0);
+    };
     for (int u = threadIdx.x; u < n_units; u += kOrderThreads) {
         const int len = unit_len(u);
         if (len > 0) atomicAdd(&hist[min(len, kOrderMaxLen)], 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // start of each length's slots, longest first
-        int run = 0;
-        for (int len = kOrderMaxLen; len >= 1; --len) {
-            const int c = hist[len];
-            hist[len] = run;
-            run += c;
+    {
+        // start of each length's slots, longest first: thread t holds length
+        // kOrderMaxLen - t, an exclusive scan over the block (warp scans, then the warp
+        // totals)
+        static_assert(kOrderThreads == kOrderMaxLen, "one length per thread");
+        __shared__ int wsum[kOrderThreads / 32];
+        const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+        const int len = kOrderMaxLen - t;
+        const int c = hist[len];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        order[n_units] = run;
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += v;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const int start = (warp > 0 ? wsum[warp - 1] : 0) + incl - c;
+        hist[len] = start;
+        if (t == kOrderThreads - 1) {
+            order[n_units] = start + c;
+            order[n_units + 1] = tps;
+            order[n_units + 2] = s_split;
+        }
     }
     __syncthreads();
     for (int u = threadIdx.x; u < n_units; u += kOrderThreads) {
@@ -810,6 +932,7 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     const int n_tiles = (g.max_ctx + kTileKeys - 1) / kTileKeys;
     const long long items = (long long)B * Hkv * g.n_rg;
     int tps;
+    bool dyn = false;
     if (num_splits > 0) {
         tps = n_tiles > 0 ? (n_tiles + num_splits - 1) / num_splits : 1;
     } else if (n_tiles == 0) {
@@ -823,22 +946,14 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
             if (c < best_cost) { best_cost = c; best = s; }
         }
         tps = (n_tiles + best - 1) / best;
-        if (page_size != 0 && items > 148) {
-            // A ragged paged batch of several waves is dispatched longest unit first, so
-            // its span is about max(longest unit, total tiles / SMs) plus per-CTA fill
-            // and the combine.  With lengths taken as uniform up to max_ctx: when the
-            // longest possible unit is within a quarter of the per-SM share, one split
-            // (no partial states, no combine) is best; otherwise units are cut at the
-            // share (at least 64 tiles), so only the longest sequences are split.
-            const long long total = items * (long long)(n_tiles + 1) / 2;
-            const long long share = (total + 147) / 148;
-            if (n_tiles + 1 <= share + share / 4) {
-                tps = n_tiles;
-            } else {
-                tps = (int)share;
-                if (tps < 64) tps = 64;
-                if (tps > n_tiles) tps = n_tiles;
-            }
+        if (page_size != 0 && items > 148 && n_tiles + 1 <= kOrderMaxLen) {
+            // A ragged paged batch of several waves: the prep kernel picks the split
+            // length per call (this one times 1, 2, 4, ...) from the sequences that are
+            // active, and the units go out longest first.  The finest length is 64
+            // tiles, or an eighth of the longest context if that is longer.
+            tps = max(64, (n_tiles + 7) / 8);
+            if (tps > n_tiles) tps = n_tiles;
+            dyn = true;
         } else if (page_size != 0 && tps < 64 && n_tiles > 64) {
             // shorter sequences of a paged batch leave their later splits empty (those
             // CTAs exit at once), so keep splits long enough to amortise a CTA
@@ -855,6 +970,7 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     // is a counting sort over lengths of at most tiles_per_split + 1 tiles.
     g.lpt = (page_size != 0 && (long long)B * Hkv * g.n_rg * g.n_splits > 148 && tps + 1 <= kOrderMaxLen &&
              (long long)B * Hkv * g.n_rg * g.n_splits <= kOrderMaxUnits) ? 1 : 0;
+    g.lpt_dyn = (g.lpt && dyn) ? 1 : 0;
     return true;
 }
 
@@ -879,7 +995,7 @@ size_t attn_workspace_bytes(const AttnGeom& g) {
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
     size_t tk = ((size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
     const size_t units = (size_t)g.B * g.Hkv * g.n_rg * g.n_splits;
-    return acc + ml + tk + (g.lpt ? (units + 1) * sizeof(int32_t) : 0) + 256;
+    return acc + ml + tk + (g.lpt ? (units + 3) * sizeof(int32_t) : 0) + 256;
 }
 
 cudaError_t attn_split_prepare(int D) {
@@ -916,8 +1032,9 @@ cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cu
 cudaError_t launch_attn_merge(const AttnMergeParams& p, cudaStream_t stream) {
     const AttnGeom& g = p.g;
     const long long rows = (long long)g.B * g.S * g.Hq;
-    const long long blocks = (rows + 7) / 8;
+    long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (p.order != nullptr && blocks > 148 * 4) blocks = 148 * 4;  // one resident wave
     const bool few = g.n_splits <= 4;
     if (g.D == 128)
         return few ? launch_pdl(attn_merge_kernel<128, 4>, dim3((unsigned)blocks), dim3(256), 0, stream, p)

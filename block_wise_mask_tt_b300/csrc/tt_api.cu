@@ -249,6 +249,7 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     if (g.n_splits > 1 && !g.inline_merge) {
         tti::AttnMergeParams mp;
         mp.g = g;
+        mp.order = order;
         mp.ctx_len = sp.ctx_len;
         mp.skip_if_zero = skip_if_zero;
         mp.part_acc = part_acc;

@@ -153,6 +153,8 @@ struct AttnGeom {
     int tiles_per_split;  // 128-token tiles per split
     int inline_merge;     // 1: the last split CTA of a row group merges (n_splits <= 4)
     int lpt;              // 1: work units dispatched longest first (ragged paged batches)
+    int lpt_dyn;          // lpt: the prep kernel picks the split length per call from the
+                          // active sequences (tiles_per_split times 1, 2, 4, ...)
     float scale_log2;     // softmax_scale * log2(e)
 };
 constexpr int kAttnInlineMergeMax = 4;  // most splits the split kernel merges itself
@@ -202,6 +204,7 @@ cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cu
 
 struct AttnMergeParams {
     AttnGeom g;
+    const int32_t* order;        // lpt: the prep kernel's output (split length, any split)
     const int32_t* ctx_len;
     const int32_t* skip_if_zero;
     const float* part_acc;

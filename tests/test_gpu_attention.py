@@ -105,6 +105,22 @@ def test_ragged_paged_longest_first(tt, splits):
     check_attention(O, Or, lse, lr, what=f"splits={splits}")
 
 
+@pytest.mark.parametrize("n_long", [0, 4])
+def test_ragged_paged_split_chosen_per_call(tt, n_long):
+    """More row groups than SMs in a ragged paged batch: the prep kernel chooses the
+    split length from the sequences' actual lengths.  All short: every row group in one
+    split, written directly.  Four long ones among 76 short: the long ones are cut into
+    64-tile units and merged by the combine pass, the short ones still written directly."""
+    w = W(B=80, L=16384, L_min=1, S=16, Hq=4, Hkv=2, D=64, paged=True, softmax_scale=0.125)
+    rng = np.random.default_rng(21 + n_long)
+    ctx = rng.integers(200, 700, size=w.B).astype(np.int32)
+    ctx[rng.choice(w.B, size=n_long, replace=False)] = rng.integers(14000, 16385, size=n_long)
+    inp = synth.make_attention_inputs(w, seed=16, ctx_len=ctx)
+    O, lse = run_attn(tt, w, inp)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr, what=f"{n_long} long sequences")
+
+
 def test_paged_equals_contiguous(tt):
     w = W(B=3, L=500, L_min=1, S=16, Hq=32, Hkv=2, D=128, paged=True, q_prescale=1 / math.sqrt(128))
     inp = synth.make_attention_inputs(w, seed=12)
