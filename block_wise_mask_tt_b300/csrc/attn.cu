@@ -965,7 +965,6 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     g.n_splits = n_tiles > 0 ? (n_tiles + tps - 1) / tps : 1;
     if (g.n_splits > 65535) { *why = "too many context splits"; return false; }
     if ((long long)B * Hkv * g.n_rg * g.n_splits > 0x7fffffffLL) { *why = "too many work units"; return false; }
-    g.inline_merge = 0;
     // Ragged batches spanning several waves: units dispatched longest first.  The sort
     // is a counting sort over lengths of at most tiles_per_split + 1 tiles.
     g.lpt = (page_size != 0 && (long long)B * Hkv * g.n_rg * g.n_splits > 148 && tps + 1 <= kOrderMaxLen &&
@@ -975,27 +974,24 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
 }
 
 // Workspace: fp32 partial accumulators [B][Hkv][n_splits][R][D], then (m, l) pairs,
-// then one counter word per row group [B][Hkv][n_rg] (zero on entry, left at zero).
-void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket,
-                 int32_t** order) {
+// then (ragged batches) the work order: units + 3 words.  Nothing in it carries over
+// from one call to the next.
+void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, int32_t** order) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
-    size_t tk = ((size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
     char* w = static_cast<char*>(ws);
     *part_acc = reinterpret_cast<float*>(w);
     *part_ml = reinterpret_cast<float*>(w + acc);
-    *ticket = reinterpret_cast<unsigned*>(w + acc + ml);
-    *order = g.lpt ? reinterpret_cast<int32_t*>(w + acc + ml + tk) : nullptr;
+    *order = g.lpt ? reinterpret_cast<int32_t*>(w + acc + ml) : nullptr;
 }
 
 size_t attn_workspace_bytes(const AttnGeom& g) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
-    size_t tk = ((size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
     const size_t units = (size_t)g.B * g.Hkv * g.n_rg * g.n_splits;
-    return acc + ml + tk + (g.lpt ? (units + 3) * sizeof(int32_t) : 0) + 256;
+    return acc + ml + (g.lpt ? (units + 3) * sizeof(int32_t) : 0) + 256;
 }
 
 cudaError_t attn_split_prepare(int D) {

@@ -18,7 +18,8 @@ namespace tti {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kIdsPerCta = 8192;
+constexpr int kMaxIdsPerCta = 8192;
+constexpr int kRows = 4;  // positions of one sequence per CTA
 
 __device__ __forceinline__ uint32_t m3(uint32_t key, uint32_t seed) {
     uint32_t k = key * 0xCC9E2D51u;
@@ -36,17 +37,23 @@ __device__ __forceinline__ uint32_t m3(uint32_t key, uint32_t seed) {
     return h;
 }
 
-// MurmurHash3_x86_32 of a 4-byte key whose first multiplication (key * c1) has
-// already been done: the vocabulary loop advances k by c1 per id instead of
-// multiplying (exact in 32-bit arithmetic).
-__device__ __forceinline__ uint32_t m3_premul(uint32_t k, uint32_t seed) {
-    k = __funnelshift_l(k, k, 15);
+// The hash of id v under a row's seed h0, split so that the work on the key alone is
+// shared by every row: with k' = rotl(v * c1, 15) * c2 the mixing step is
+// rotl(h0 ^ k', 13) = rotl(h0, 13) ^ rotl(k', 13) (a rotation distributes over xor), so
+// key_part(v) = rotl(k', 13) is computed once per id and seed_part(h0) = rotl(h0, 13)
+// once per row.  The length xor (h ^= 4, then h ^= h >> 16) is taken as
+// h ^ (h >> 16) ^ 4, since the 4 does not reach the shifted bits.  Exact in 32-bit
+// arithmetic: the same value as m3(v, h0).
+__device__ __forceinline__ uint32_t key_part(uint32_t k_premul) {
+    uint32_t k = __funnelshift_l(k_premul, k_premul, 15);
     k *= 0x1B873593u;
-    uint32_t h = seed ^ k;
-    h = __funnelshift_l(h, h, 13);
+    return __funnelshift_l(k, k, 13);
+}
+__device__ __forceinline__ uint32_t seed_part(uint32_t h0) { return __funnelshift_l(h0, h0, 13); }
+__device__ __forceinline__ uint32_t m3_split(uint32_t key, uint32_t seed) {
+    uint32_t h = seed ^ key;
     h = h * 5u + 0xE6546B64u;
-    h ^= 4u;  // key length in bytes
-    h ^= h >> 16;
+    h = h ^ (h >> 16) ^ 4u;
     h *= 0x85EBCA6Bu;
     h ^= h >> 13;
     h *= 0xC2B2AE35u;
@@ -55,61 +62,94 @@ __device__ __forceinline__ uint32_t m3_premul(uint32_t k, uint32_t seed) {
 }
 
 __device__ __forceinline__ float noise(uint32_t r) {
-    const int sum = (int)__dp4a(r, 0x01010101u, 0u);  // sum of the four bytes
+    // sum of the four bytes minus 510, the offset taken as the dot product's addend
+    const int sum = (int)__dp4a(r, 0x01010101u, (uint32_t)-510);
     // fp32(1/sqrt(4*(256^2-1)/12)) = 0x3BDDB446
-    return __fmul_rn(__int2float_rn(sum - 510), __uint_as_float(0x3BDDB446u));
+    return __fmul_rn(__int2float_rn(sum), __uint_as_float(0x3BDDB446u));
 }
 
+// One CTA: a chunk of ids_per_cta ids of kRows consecutive positions of one sequence.
+// The per-id key work is shared by the CTA's masked rows.
 __global__ void __launch_bounds__(kThreads) logits_kernel(LogitsParams p) {
     ttk::pdl_wait();
     ttk::pdl_trigger();
-    const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
-    const int row = b * p.S + s;
-    if (p.ids != nullptr && __ldg(p.ids + row) != p.mask_id) return;
+    const int c = blockIdx.x, s0 = blockIdx.y * kRows, b = blockIdx.z;
     const uint32_t step = p.steps ? (uint32_t)__ldg(p.steps + b) : 0u;
     const uint32_t seed = p.dyn ? p.dyn[0] : p.seed;
     const uint32_t block = p.dyn ? p.dyn[1] : (uint32_t)p.block_index;
-    uint32_t h = m3((uint32_t)b, seed);
-    h = m3(block, h);
-    h = m3(step, h);
-    h = m3((uint32_t)s, h);
-    uint32_t planted = m3(0xFFFFFFFFu, h) % (uint32_t)p.V;
-    if ((int)planted == p.mask_id) planted = (planted + 1u) % (uint32_t)p.V;
-    const float u = __fmul_rn((float)(m3(0xFFFFFFFEu, h) >> 8), 5.9604644775390625e-08f);
-    float lo = p.boost_lo, hi = p.boost_hi;
-    if (p.kind == 1) {
-        const bool upper = (m3(0xFFFFFFFDu, h) & 1u) != 0u;
-        lo = upper ? 10.0f : 0.0f;
-        hi = upper ? 20.0f : 4.0f;
+    // Row r's hash chain and planted id, computed by thread r and shared
+    __shared__ uint32_t s_hs[kRows], s_planted[kRows];
+    __shared__ float s_boost[kRows];
+    __shared__ int s_act[kRows];
+    if (threadIdx.x < kRows) {
+        const int r = threadIdx.x, s = s0 + r;
+        uint32_t h = m3((uint32_t)b, seed);
+        h = m3(block, h);
+        h = m3(step, h);
+        h = m3((uint32_t)s, h);
+        s_act[r] = (s < p.S && (p.ids == nullptr || __ldg(p.ids + b * p.S + s) == p.mask_id)) ? 1 : 0;
+        s_hs[r] = seed_part(h);
+        uint32_t pl = m3(0xFFFFFFFFu, h) % (uint32_t)p.V;
+        if ((int)pl == p.mask_id) pl = (pl + 1u) % (uint32_t)p.V;
+        s_planted[r] = pl;
+        const float u = __fmul_rn((float)(m3(0xFFFFFFFEu, h) >> 8), 5.9604644775390625e-08f);
+        float lo = p.boost_lo, hi = p.boost_hi;
+        if (p.kind == 1) {
+            const bool upper = (m3(0xFFFFFFFDu, h) & 1u) != 0u;
+            lo = upper ? 10.0f : 0.0f;
+            hi = upper ? 20.0f : 4.0f;
+        }
+        s_boost[r] = __fadd_rn(lo, __fmul_rn(u, __fsub_rn(hi, lo)));
     }
-    const float boost = __fadd_rn(lo, __fmul_rn(u, __fsub_rn(hi, lo)));
+    __syncthreads();
+    bool act[kRows];
+    uint32_t hs[kRows], planted[kRows];
+    float boost[kRows];
+    bool any = false;
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        act[r] = s_act[r] != 0;
+        any |= act[r];
+        hs[r] = s_hs[r];
+        planted[r] = s_planted[r];
+        boost[r] = s_boost[r];
+    }
+    if (!any) return;
 
-    float* rowp = p.logits + (size_t)row * p.V;
-    const int v0 = c * kIdsPerCta;
-    const int v1 = min(p.V, v0 + kIdsPerCta);
+    float* rows = p.logits + (size_t)(b * p.S + s0) * p.V;
+    const int v0 = c * p.ids_per_cta;
+    const int v1 = min(p.V, v0 + p.ids_per_cta);
+    constexpr uint32_t kC1 = 0xCC9E2D51u;
     if ((p.V & 3) == 0) {
-        constexpr uint32_t kC1 = 0xCC9E2D51u;
         for (int v = v0 + 4 * threadIdx.x; v < v1; v += 4 * kThreads) {
             const uint32_t k0 = (uint32_t)v * kC1;
-            float4 o;
-            o.x = noise(m3_premul(k0, h));
-            o.y = noise(m3_premul(k0 + kC1, h));
-            o.z = noise(m3_premul(k0 + 2u * kC1, h));
-            o.w = noise(m3_premul(k0 + 3u * kC1, h));
-            const unsigned d = planted - (uint32_t)v;
-            if (d < 4u) {  // the planted id is in this group of four
-                if (d == 0) o.x = __fadd_rn(o.x, boost);
-                if (d == 1) o.y = __fadd_rn(o.y, boost);
-                if (d == 2) o.z = __fadd_rn(o.z, boost);
-                if (d == 3) o.w = __fadd_rn(o.w, boost);
+            const uint32_t kp[4] = {key_part(k0), key_part(k0 + kC1), key_part(k0 + 2u * kC1),
+                                    key_part(k0 + 3u * kC1)};
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                if (!act[r]) continue;
+                float o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = noise(m3_split(kp[e], hs[r]));
+                const unsigned d = planted[r] - (uint32_t)v;
+                if (d < 4u) {  // the planted id is in this group of four
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (d == (unsigned)e) o[e] = __fadd_rn(o[e], boost[r]);
+                }
+                *reinterpret_cast<float4*>(rows + (size_t)r * p.V + v) = make_float4(o[0], o[1], o[2], o[3]);
             }
-            *reinterpret_cast<float4*>(rowp + v) = o;
         }
     } else {
         for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
-            float z = noise(m3((uint32_t)v, h));
-            if (v == (int)planted) z = __fadd_rn(z, boost);
-            rowp[v] = z;
+            const uint32_t kp = key_part((uint32_t)v * kC1);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                if (!act[r]) continue;
+                float z = noise(m3_split(kp, hs[r]));
+                if (v == (int)planted[r]) z = __fadd_rn(z, boost[r]);
+                rows[(size_t)r * p.V + v] = z;
+            }
         }
     }
 }
@@ -127,8 +167,15 @@ cudaError_t launch_set_logits_dyn(uint32_t* dyn, uint32_t seed, int block_index,
     return launch_pdl(set_dyn_kernel, dim3(1), dim3(1), 0, stream, dyn, seed, (uint32_t)block_index);
 }
 
-cudaError_t launch_logits(const LogitsParams& p, cudaStream_t stream) {
-    dim3 grid((p.V + kIdsPerCta - 1) / kIdsPerCta, p.S, p.B);
+cudaError_t launch_logits(const LogitsParams& p_in, cudaStream_t stream) {
+    // 8192 ids per CTA; small batches take smaller chunks (down to 1024) so that the
+    // grid still covers every SM about twice
+    LogitsParams p = p_in;
+    const long long groups = (long long)((p.S + kRows - 1) / kRows) * p.B;
+    p.ids_per_cta = kMaxIdsPerCta;
+    while (p.ids_per_cta > 1024 && groups * ((p.V + p.ids_per_cta - 1) / p.ids_per_cta) < 2LL * 148)
+        p.ids_per_cta >>= 1;
+    dim3 grid((p.V + p.ids_per_cta - 1) / p.ids_per_cta, (p.S + kRows - 1) / kRows, p.B);
     return launch_pdl(logits_kernel, grid, dim3(kThreads), 0, stream, p);
 }
 

@@ -205,10 +205,9 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     }
     float* part_acc = nullptr;
     float* part_ml = nullptr;
-    unsigned* ticket = nullptr;
     int32_t* order = nullptr;
     if (!pl.has_ctx) g.lpt = 0;
-    tti::attn_layout(g, ws, &part_acc, &part_ml, &ticket, &order);
+    tti::attn_layout(g, ws, &part_acc, &part_ml, &order);
     // Epilogue store maps: partial states when the context is split and a second pass
     // combines them; the output itself wherever a CTA may write it directly (when G
     // divides 128, so that a 128-row tile covers whole positions).
@@ -216,7 +215,7 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     maps.part = maps.kb;  // placeholders for the maps that are not used
     maps.out = maps.kb;
     maps.out_tma = 0;
-    if (g.n_splits > 1 && !g.inline_merge) {
+    if (g.n_splits > 1) {
         const cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.R,
                                     (cuuint64_t)g.B * g.Hkv * g.n_splits};
         const cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)g.R * g.D * 4};
@@ -239,14 +238,13 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     sp.skip_if_zero = skip_if_zero;
     sp.part_acc = part_acc;
     sp.part_ml = part_ml;
-    sp.ticket = ticket;
     sp.order = order;
     sp.out = static_cast<uint16_t*>(out);
     sp.lse = lse;
     sp.err = err;
     if (order != nullptr) TT_CUDA(tti::launch_attn_order(sp, st));
     TT_CUDA(tti::launch_attn_split(sp, maps, st));
-    if (g.n_splits > 1 && !g.inline_merge) {
+    if (g.n_splits > 1) {
         tti::AttnMergeParams mp;
         mp.g = g;
         mp.order = order;

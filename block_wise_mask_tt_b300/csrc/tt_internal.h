@@ -57,6 +57,7 @@ struct LogitsParams {
     int kind;
     float boost_lo, boost_hi;
     const uint32_t* dyn;   // nullable: {seed, block_index} read on the device instead
+    int ids_per_cta;       // set by launch_logits
 };
 cudaError_t launch_logits(const LogitsParams& p, cudaStream_t stream);
 cudaError_t launch_set_logits_dyn(uint32_t* dyn, uint32_t seed, int block_index, cudaStream_t stream);
@@ -151,13 +152,11 @@ struct AttnGeom {
     int max_pages, num_pages;
     int n_splits;
     int tiles_per_split;  // 128-token tiles per split
-    int inline_merge;     // 1: the last split CTA of a row group merges (n_splits <= 4)
     int lpt;              // 1: work units dispatched longest first (ragged paged batches)
     int lpt_dyn;          // lpt: the prep kernel picks the split length per call from the
                           // active sequences (tiles_per_split times 1, 2, 4, ...)
     float scale_log2;     // softmax_scale * log2(e)
 };
-constexpr int kAttnInlineMergeMax = 4;  // most splits the split kernel merges itself
 constexpr int kOrderMaxLen = 1024;       // longest unit (tiles) the longest-first order sorts
 constexpr int kOrderMaxUnits = 1 << 20;  // most work units it sorts
 bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_size,
@@ -165,8 +164,9 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
                    AttnGeom& g, const char** why);
 size_t attn_workspace_bytes(const AttnGeom& g);
 // Pointers into a workspace of attn_workspace_bytes(g) bytes.  order (lpt only):
-// the work units sorted by length, then their count.
-void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket,
+// the work units sorted by length, then their count, the split length of the call and
+// a flag that is 1 when some row group was split.
+void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml,
                  int32_t** order);
 
 struct AttnSplitParams {
@@ -177,10 +177,9 @@ struct AttnSplitParams {
     const int32_t* skip_if_zero; // nullable
     float* part_acc;             // [B][Hkv][n_splits][R][D]
     float* part_ml;              // [B][Hkv][n_splits][R][2]
-    unsigned int* ticket;        // [B][Hkv][n_rg]: zero on entry and on exit (inline merge)
     const int32_t* order;        // lpt: [units] work unit of each CTA, then the count
-    uint16_t* out;               // bf16 [B][S][Hq][D]: written here when n_splits == 1 or
-                                 // when the split kernel merges (inline_merge)
+    uint16_t* out;               // bf16 [B][S][Hq][D]: written here by the CTAs of row
+                                 // groups with one non-empty split
     float* lse;                  // nullable, [B][S][Hq]: likewise
     int* err;
 };
