@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 0) ttk::report_error(p.err, ttk::kErrDevice);
             if (!direct) {
                 for (int r = tid; r < g.rows_per_cta; r += kThreads) {
-                    const int rglob = rg * 256 + r;
+                    const int rglob = rg * g.rows_per_cta + r;
                     if (rglob < g.R) {
                         const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + rglob;
                         p.part_ml[2 * pi + 0] = -CUDART_INF_F;
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_row = tid & 127;        // TMEM lane (tile row) of this softmax thread
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int r_local = mt * 128 + lane_row;               // row within this CTA
-    const int r_glob = rg * 256 + r_local;                 // packed row of (b, gkv)
+    const int r_glob = rg * g.rows_per_cta + r_local;      // packed row of (b, gkv)
     const bool in_tile = q >= 0 && mt < n_mt;
     const bool row_valid = in_tile && r_local < g.rows_per_cta && r_glob < g.R;
 
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(3, 256 * n_mt);  // every row of every tile is staged
             if (q == 0 && lane_row == 0) {
                 for (int t = 0; t < n_mt; ++t) {
-                    const int row0 = rg * 256 + t * 128;
+                    const int row0 = rg * g.rows_per_cta + t * 128;
                     for (int bx = 0; bx < nb; ++bx) {
                         const uint32_t src = ttk::smem_u32(smem + (size_t)(t * nb + bx) * 16384);
                         if (direct)
@@ -930,6 +930,14 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     if (!(softmax_scale > 0.f) || !(softmax_scale < 1e30f)) { *why = "softmax_scale must be positive and finite"; return false; }
     g.scale_log2 = softmax_scale * kLog2e;
     const int n_tiles = (g.max_ctx + kTileKeys - 1) / kTileKeys;
+    if (g.R > 128 && (long long)B * Hkv * g.n_rg * (n_tiles + 1) <= 148LL * 8) {
+        // A problem of a few 128-key rounds per SM in all is latency-bound: one 128-row
+        // tile per CTA halves each round's tensor work and doubles the CTAs (the second
+        // row tile's CTA finds the same K/V tiles in L2).
+        g.rows_per_cta = 128;
+        g.n_rg = (g.R + 127) / 128;
+        g.n_mt = 1;
+    }
     const long long items = (long long)B * Hkv * g.n_rg;
     int tps;
     bool dyn = false;

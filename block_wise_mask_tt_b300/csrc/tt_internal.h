@@ -144,8 +144,8 @@ cudaError_t launch_qkv(const QkvParams& p, const LmHeadMaps& maps, cudaStream_t 
 struct AttnGeom {
     int B, S, Hq, Hkv, G, D;
     int R;             // G * S packed query rows per (sequence, kv head), row = s * G + j
-    int rows_per_cta;  // min(R, 256): rows one split CTA serves (one or two 128-row tiles)
-    int n_rg;          // row groups per (sequence, kv head): ceil(R / 256)
+    int rows_per_cta;  // rows one split CTA serves: min(R, 256), or 128 on small problems
+    int n_rg;          // row groups per (sequence, kv head): ceil(R / rows_per_cta)
     int n_mt;          // 128-row MMA tiles per CTA: ceil(rows_per_cta / 128)
     int max_ctx;       // contiguous: token stride; paged: max_pages * page_size
     int page_size;     // 0 or 64

@@ -49,10 +49,13 @@ def check_qkv(y, W, q, k, v, Hq, Hkv, D, what=""):
 
 CASES = [
     # (B, S, H, Hq, Hkv, D): one and several 128-row tiles, a partial 64-slice of H,
-    # column segments of 64 and 128 lanes
+    # column segments of 64 and 128 lanes, and 74 / 75 single-unit work items (half the
+    # SMs of the part and one more)
     (1, 16, 2688, 32, 2, 128),
     (3, 16, 256, 4, 1, 64),
     (20, 16, 200, 8, 2, 64),
+    (1, 8, 512, 72, 1, 64),
+    (1, 8, 512, 73, 1, 64),
     (9, 32, 512, 16, 4, 128),
     (1, 1, 64, 1, 1, 64),
 ]
