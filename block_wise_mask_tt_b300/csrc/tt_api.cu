@@ -13,11 +13,23 @@
 #include <vector>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "tt.h"
 #include "tt_internal.h"
 
 namespace {
+
+// An NVTX range over one entry point (its validation and enqueue on the host), so that
+// a profiler's timeline names every call and step.  With no tool attached the push and
+// pop return at once.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define TT_RANGE(name) const NvtxRange tt_nvtx_range_(name)
 
 // First error code reported by any libtt kernel on this device (see tt_device_status).
 __device__ int g_tt_device_error;
@@ -716,6 +728,7 @@ tt_status tt_device_status(int reset) {
 tt_status tt_adaln_modulate(const void* x, const float* shift, const float* scale,
                             const int32_t* row_index, int table_rows, void* y, int B, int S, int H,
                             float eps, tt_stream_t stream) {
+    TT_RANGE("tt_adaln_modulate");
     if (B < 1 || S < 1 || H < 1) return fail(TT_ERR_INVALID_ARG, "B, S, H must be positive");
     if (H % 8 != 0) return fail(TT_ERR_UNSUPPORTED, "H must be a multiple of 8");
     if (H > tti::kAdalnMaxH) return fail(TT_ERR_UNSUPPORTED, "H must be at most %d", tti::kAdalnMaxH);
@@ -756,6 +769,7 @@ tt_status tt_denoise_attn(const tt_attn_dims* dims, const void* q, const void* k
                           const void* v_blk, const void* k_ctx, const void* v_ctx,
                           const int32_t* page_table, const int32_t* ctx_len, void* out, float* lse,
                           void* workspace, size_t workspace_bytes, tt_stream_t stream) {
+    TT_RANGE("tt_denoise_attn");
     AttnPlan pl;
     TT_TRY(plan_attn(dims, q, k_blk, v_blk, k_ctx, v_ctx, page_table, ctx_len, out, pl));
     if (lse != nullptr) TT_TRY(need_ptr(lse, "lse", false));
@@ -769,6 +783,7 @@ tt_status tt_denoise_attn(const tt_attn_dims* dims, const void* q, const void* k
 tt_status tt_synthetic_logits(const tt_logits_spec* spec, const int32_t* ids, const int32_t* steps,
                               float* logits, int B, int S, int V, int32_t mask_id,
                               tt_stream_t stream) {
+    TT_RANGE("tt_synthetic_logits");
     if (spec == nullptr) return fail(TT_ERR_INVALID_ARG, "spec is null");
     TT_TRY(check_vocab(B, S, V));
     if (spec->kind != 0 && spec->kind != 1) return fail(TT_ERR_INVALID_ARG, "kind must be 0 or 1");
@@ -800,6 +815,7 @@ tt_status tt_confidence_unmask(const float* logits, int32_t* ids, int32_t* n_mas
                                float* conf, uint8_t* commit, uint8_t* commit_step, int B, int S,
                                int V, int32_t mask_id, float gamma, int max_steps, void* workspace,
                                size_t workspace_bytes, tt_stream_t stream) {
+    TT_RANGE("tt_confidence_unmask");
     TT_TRY(check_vocab(B, S, V));
     if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
     if (max_steps < 1 || max_steps > 255) return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
@@ -836,6 +852,7 @@ tt_status tt_sampler_unmask(const float* logits, int32_t* ids, int32_t* n_masked
                             float* conf, uint8_t* commit, uint8_t* commit_step, int B, int S, int V,
                             int32_t mask_id, const tt_sampler* sampler, void* workspace,
                             size_t workspace_bytes, tt_stream_t stream) {
+    TT_RANGE("tt_sampler_unmask");
     TT_TRY(check_sampler(sampler));
     TT_TRY(check_vocab(B, S, V));
     if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
@@ -871,6 +888,7 @@ tt_status tt_confidence_unmask_noalloc(const float* logits, int32_t* ids, int32_
                                        int32_t* steps, float* conf, uint8_t* commit,
                                        uint8_t* commit_step, int B, int S, int V, int32_t mask_id,
                                        float gamma, int max_steps, tt_stream_t stream) {
+    TT_RANGE("tt_confidence_unmask_noalloc");
     TT_TRY(check_vocab(B, S, V));
     if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
     if (max_steps < 1 || max_steps > 255) return fail(TT_ERR_INVALID_ARG, "max_steps must be in [1, 255]");
@@ -921,6 +939,7 @@ size_t tt_denoise_workspace(const tt_step_desc* desc) {
 
 tt_status tt_denoise_step(const tt_step_desc* desc, const tt_step_tensors* t, void* workspace,
                           size_t workspace_bytes, tt_stream_t stream) {
+    TT_RANGE("tt_denoise_step");
     StepPlan sp;
     TT_TRY(plan_step(desc, sp));
     TT_TRY(check_step_tensors(desc, t));
@@ -934,6 +953,7 @@ tt_status tt_denoise_step(const tt_step_desc* desc, const tt_step_tensors* t, vo
 
 tt_status tt_denoise_block_loop(const tt_step_desc* desc, const tt_step_tensors* t, void* workspace,
                                 size_t workspace_bytes, tt_stream_t stream) {
+    TT_RANGE("tt_denoise_block_loop");
     StepPlan sp;
     TT_TRY(plan_step(desc, sp));
     TT_TRY(check_step_tensors(desc, t));
@@ -968,6 +988,7 @@ tt_status tt_append_block(const tt_attn_dims* dims, const void* k_blk, const voi
                           const int32_t* ids, const tt_stop_spec* stop, int32_t* generated,
                           uint8_t* done, int32_t* out_tokens, int out_stride, int out_offset,
                           tt_stream_t stream) {
+    TT_RANGE("tt_append_block");
     tti::AttnGeom g;
     TT_TRY(check_attn(dims, g));
     if (stop == nullptr) return fail(TT_ERR_INVALID_ARG, "stop is null");
@@ -1018,6 +1039,7 @@ tt_status tt_generate(const tt_step_desc* desc, const tt_step_tensors* t, int n_
                       const tt_stop_spec* stop, int32_t* generated, uint8_t* done,
                       int32_t* out_tokens, void* workspace, size_t workspace_bytes,
                       tt_stream_t stream) {
+    TT_RANGE("tt_generate");
     if (desc == nullptr || t == nullptr || stop == nullptr)
         return fail(TT_ERR_INVALID_ARG, "desc, tensors and stop must be given");
     if (n_blocks < 1) return fail(TT_ERR_INVALID_ARG, "n_blocks must be >= 1");
@@ -1051,6 +1073,7 @@ tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32_t* ids
                            int32_t* steps, float* conf, uint8_t* commit, uint8_t* commit_step, int B,
                            int S, int H, int V, int32_t mask_id, const tt_sampler* sampler,
                            void* workspace, size_t workspace_bytes, tt_stream_t stream) {
+    TT_RANGE("tt_lmhead_unmask");
     TT_TRY(check_lmhead(B, S, H, V));
     TT_TRY(check_sampler(sampler));
     if (mask_id < 0 || mask_id >= V) return fail(TT_ERR_INVALID_ARG, "mask_id outside the vocabulary");
@@ -1070,6 +1093,7 @@ tt_status tt_lmhead_unmask(const void* hidden, const void* w_vocab, int32_t* ids
 
 tt_status tt_qkv_project(const void* y, const void* w_qkv, void* q, void* k_blk, void* v_blk, int B, int S,
                          int H, int Hq, int Hkv, int D, tt_stream_t stream) {
+    TT_RANGE("tt_qkv_project");
     TT_TRY(check_qkv(B, S, H, Hq, Hkv, D));
     TT_TRY(need_ptr(y, "y"));
     TT_TRY(need_ptr(w_qkv, "w_qkv"));
@@ -1082,6 +1106,7 @@ tt_status tt_qkv_project(const void* y, const void* w_qkv, void* q, void* k_blk,
 }
 
 tt_status tt_selftest_wait_timeout(uint32_t limit_us, tt_stream_t stream) {
+    TT_RANGE("tt_selftest_wait_timeout");
     if (limit_us < 1 || limit_us > 1000000u)
         return fail(TT_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
     int* err = nullptr;
