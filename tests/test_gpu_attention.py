@@ -121,6 +121,17 @@ def test_ragged_paged_split_chosen_per_call(tt, n_long):
     check_attention(O, Or, lse, lr, what=f"{n_long} long sequences")
 
 
+def test_small_ragged_batch_in_128_row_groups(tt):
+    """Short contexts over many sequences: a few tile-rounds per SM in all, so each CTA
+    serves one 128-row tile (here R = 256 rows per kv head, two groups), and with more
+    row groups than SMs the prep kernel orders them and picks the split length."""
+    w = W(B=100, L=512, L_min=64, S=16, Hq=32, Hkv=2, D=64, paged=True, softmax_scale=0.125)
+    inp = synth.make_attention_inputs(w, seed=17)
+    O, lse = run_attn(tt, w, inp)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr, what="128-row groups")
+
+
 def test_paged_equals_contiguous(tt):
     w = W(B=3, L=500, L_min=1, S=16, Hq=32, Hkv=2, D=128, paged=True, q_prescale=1 / math.sqrt(128))
     inp = synth.make_attention_inputs(w, seed=12)
