@@ -9,7 +9,9 @@
 //   * the rows are the packed (block position s, query head j of the GQA group)
 //     pairs, row = s*G + j.  One CTA serves up to 256 of them as one or two 128-row
 //     MMA tiles, so every K/V tile it loads feeds G*S query rows and QK^T / PV are
-//     dense contractions (M = 128, N = 128 keys, K = D for QK^T; N = D, K = 128 for PV);
+//     dense contractions (M = 128, N = 128 keys, K = D for QK^T; N = D, K = 128 for PV).
+//     A call of only a few key tiles per SM in all is latency-bound and takes one
+//     128-row tile per CTA instead (twice the CTAs, half the work per round);
 //   * split 0 also takes the block's own S keys, as one extra (masked) key tile in
 //     front of its context tiles, so the block keys run on the tensor cores too;
 //   * warp 0 streams 128-token K/V tiles (two 64-row TMA boxes each, so a tile may
@@ -29,9 +31,12 @@
 //     matrix products;
 //   * the running max is raised (and O rescaled in TMEM) only when it grows by more
 //     than 2^8, so most tiles need no correction;
-//   * with a single split the CTA writes the normalised output (bf16) and the lse
-//     itself; otherwise each row's partial state (m, l, O) goes to the workspace and
-//     the combine pass (one warp per output row) merges them.
+//   * a CTA whose row group has one non-empty split writes the normalised output
+//     (bf16) and the lse itself; otherwise each row's partial state (m, l, O) goes to
+//     the workspace and the combine pass (one warp per output row) merges them;
+//   * on ragged paged batches of more than one wave a one-CTA prep kernel picks the
+//     call's split length from the active sequences' lengths and sorts the work units
+//     longest first; the split kernel's 1-D grid takes them in that order.
 //
 // Every wait is bounded: a wait that runs out sets the device error word, the CTA
 // drains what it issued and returns.
