@@ -15,7 +15,8 @@
 //     items = row tiles x chunks covers the CTAs once.  Per 256-id vocabulary tile:
 //     warp 0 streams the A tile (128 rows x 64 of H) and four 64-row boxes of W per
 //     64-wide slice of H into a four-stage ring (TMA, 128-byte swizzle; narrower
-//     problems use tiles of one to three boxes and up to eight stages); warp 1 issues
+//     problems use tiles of one to three boxes, fewer rows of A when there are fewer
+//     than 128, and up to 16 stages); warp 1 issues
 //     tcgen05.mma 128 x 256 x 16 into one of two TMEM accumulators (256 columns each,
 //     so the epilogue of one tile overlaps the products of the next); warps 2-5 (one
 //     TMEM lane = one row per thread) read the accumulator and fold it into the row's
@@ -46,10 +47,11 @@ using namespace um;
 constexpr uint32_t kATile = 128 * 128;                  // 128 rows x 64 bf16
 constexpr uint32_t kBBox = 64 * 128;                    // 64 vocabulary rows x 64 bf16
 constexpr uint32_t kRingBytes = 4 * (kATile + 4 * kBBox);  // four stages of the widest tile
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 constexpr uint32_t kBarOff = kRingBytes;                // barriers after the ring
-constexpr uint32_t kSlotOff = kBarOff + 256;            // TMEM address slot
-constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t kSlotOff = kBarOff + 512;            // TMEM address slot
+constexpr uint32_t kSmemBytes = kBarOff + 1024 + 1024;  // + slack for 1024-B alignment
+static_assert(8 * (2 * kMaxStages + 5) <= 512, "barriers fit before the TMEM slot");
 constexpr int kGemmThreads = 192;                       // producer, MMA, 4 epilogue warps
 constexpr int kGatherRows = 8;                          // rows copied per gather CTA (one per warp)
 
@@ -187,12 +189,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const Plan pl = make_plan(n_rows, g.N, g.n_ctas);
     const int items = pl.n_mt * pl.n_chunks;
     const int nkb = (g.H + 63) / 64;
-    // Vocabulary tiles are wbox 64-id units wide (the widest chunk needs no more); the
-    // ring then holds as many stages of A + wbox boxes as fit, up to eight, so narrow
-    // problems keep more k-slices in flight.
+    // Vocabulary tiles are wbox 64-id units wide (the widest chunk needs no more).  A
+    // stage holds the A box (maps.a_rows rows: below one 128-row tile only the rows
+    // that exist) and wbox boxes of W; the ring holds as many stages as fit, up to 16,
+    // so narrow problems keep more k-slices in flight.  The MMA reads 128 rows of A
+    // from the stage; rows past a_rows read whatever follows (their accumulator rows
+    // are never used), so the last stage keeps a whole tile of room below the ring's end.
     const int wbox = pl.n_chunks ? min(4, (pl.units + pl.n_chunks - 1) / pl.n_chunks) : 4;
-    const uint32_t stage_bytes = kATile + (uint32_t)wbox * kBBox;
-    const uint32_t n_stages = min((uint32_t)kMaxStages, kRingBytes / stage_bytes);
+    const uint32_t a_bytes = (uint32_t)maps.a_rows * 128u;
+    const uint32_t stage_bytes = a_bytes + (uint32_t)wbox * kBBox;
+    const uint32_t n_stages = min(min((uint32_t)kMaxStages, kRingBytes / stage_bytes),
+                                  (kRingBytes - kATile) / stage_bytes + 1u);
     const uint32_t idesc = ttk::idesc_bf16(128, 64 * wbox, false, false);
     bool ok = true;
 
@@ -218,8 +225,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             ok = false;
                             break;
                         }
-                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + kATile;
-                        ttk::mbar_arrive_expect_tx(full_bar(st), kATile + (uint32_t)nbox * kBBox);
+                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + a_bytes;
+                        ttk::mbar_arrive_expect_tx(full_bar(st), a_bytes + (uint32_t)nbox * kBBox);
                         ttk::tma_load_2d(sA, &maps.a, kb * 64, mt * 128, full_bar(st));
                         for (int i = 0; i < nbox; ++i)
                             ttk::tma_load_2d(sB + (uint32_t)i * kBBox, &maps.w, kb * 64, (ut + i) * 64, full_bar(st));
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             break;
                         }
                         ttk::tc_fence_after();
-                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + kATile;
+                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + a_bytes;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             ttk::mma_bf16_ss(tmem + a * 256u, ttk::sdesc_sw128(sA + 32u * k, 16, 1024),

@@ -356,7 +356,8 @@ tt_status enqueue_lmhead(const void* hidden, const void* w_vocab, int32_t* ids, 
     {
         const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)tti::lmhead_a_rows(p.rows)};
         const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-        const cuuint32_t box[2] = {64, 128};
+        maps.a_rows = tti::gemm_a_box_rows(p.rows);
+        const cuuint32_t box[2] = {64, (cuuint32_t)maps.a_rows};
         TT_TRY(encode_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a_c, dims, strides, box));
     }
     {
@@ -397,7 +398,8 @@ tt_status enqueue_qkv(const void* y, const void* w_qkv, void* q, void* k, void* 
     {
         const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)p.rows};
         const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-        const cuuint32_t box[2] = {64, 128};
+        maps.a_rows = tti::gemm_a_box_rows(p.rows);
+        const cuuint32_t box[2] = {64, (cuuint32_t)maps.a_rows};
         TT_TRY(encode_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box));
     }
     {

@@ -119,9 +119,13 @@ struct LmHeadParams {
     UnmaskParams um;       // ids, steps, outputs, sampler, row_res, ticket (decision)
 };
 struct LmHeadMaps {
-    CUtensorMap a;  // a_c: (H, B*S) bf16, box 64 x 128, 128-B swizzle
+    CUtensorMap a;  // A rows: (H, rows) bf16, box 64 x a_rows, 128-B swizzle
     CUtensorMap w;  // W: (H, V) bf16, box 64 x 64, 128-B swizzle
+    int a_rows;     // rows of the A box: 128, or the row count rounded up to 8 when below
 };
+// Rows of the GEMM's A box for a problem of at most `rows` rows: below one 128-row
+// tile only the rows that exist are copied.
+inline int gemm_a_box_rows(int rows) { return rows >= 128 ? 128 : (rows + 7) / 8 * 8; }
 size_t lmhead_a_rows(int rows);  // rows of a_c: B*S rounded up to a multiple of 128
 size_t lmhead_workspace_bytes(int B, int S, int H, int n_ctas);
 // Fills the workspace pointers of p (p.rows, p.n_ctas set by the caller).
