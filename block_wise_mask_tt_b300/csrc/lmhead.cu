@@ -197,9 +197,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // are never used), so the last stage keeps a whole tile of room below the ring's end.
     const int wbox = pl.n_chunks ? min(4, (pl.units + pl.n_chunks - 1) / pl.n_chunks) : 4;
     const uint32_t a_bytes = (uint32_t)maps.a_rows * 128u;
-    const uint32_t stage_bytes = a_bytes + (uint32_t)wbox * kBBox;
+    // One k-slice: the A box then the W boxes.  Narrow slices are grouped kps to a
+    // stage, so one barrier round trip (TMA completion, MMA commit, producer wake-up)
+    // covers kps slices of products.
+    const uint32_t slice_bytes = a_bytes + (uint32_t)wbox * kBBox;
+    const int kps = slice_bytes <= 12u * 1024u ? 4 : slice_bytes <= 24u * 1024u ? 2 : 1;
+    const uint32_t stage_bytes = (uint32_t)kps * slice_bytes;
+    // the last stage's last slice needs a whole A tile of room (see above)
+    const uint32_t tail = kATile + (uint32_t)(kps - 1) * slice_bytes;
     const uint32_t n_stages = min(min((uint32_t)kMaxStages, kRingBytes / stage_bytes),
-                                  (kRingBytes - kATile) / stage_bytes + 1u);
+                                  (kRingBytes - tail) / stage_bytes + 1u);
     const uint32_t idesc = ttk::idesc_bf16(128, 64 * wbox, false, false);
     bool ok = true;
 
@@ -214,22 +221,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t kc = 0, st = 0, ph = 0;  // k-slices issued; ring slot and lap parity
+            uint32_t kc = 0, st = 0, ph = 0;  // stages filled; ring slot and lap parity
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
                 int mt, chunk, u0, u1;
                 item_geom(item, mt, chunk, u0, u1);
                 for (int ut = u0; ut < u1 && ok; ut += wbox) {
                     const int nbox = min(wbox, u1 - ut);
-                    for (int kb = 0; kb < nkb; ++kb, ++kc) {
+                    for (int kb = 0; kb < nkb; kb += kps, ++kc) {
                         if (kc >= n_stages && !ttk::mbar_wait(empty_bar(st), ph ^ 1u)) {
                             ok = false;
                             break;
                         }
-                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + a_bytes;
-                        ttk::mbar_arrive_expect_tx(full_bar(st), a_bytes + (uint32_t)nbox * kBBox);
-                        ttk::tma_load_2d(sA, &maps.a, kb * 64, mt * 128, full_bar(st));
-                        for (int i = 0; i < nbox; ++i)
-                            ttk::tma_load_2d(sB + (uint32_t)i * kBBox, &maps.w, kb * 64, (ut + i) * 64, full_bar(st));
+                        if (kps == 1) {
+                            const uint32_t sA = sbase + st * stage_bytes, sB = sA + a_bytes;
+                            ttk::mbar_arrive_expect_tx(full_bar(st), a_bytes + (uint32_t)nbox * kBBox);
+                            ttk::tma_load_2d(sA, &maps.a, kb * 64, mt * 128, full_bar(st));
+                            for (int i = 0; i < nbox; ++i)
+                                ttk::tma_load_2d(sB + (uint32_t)i * kBBox, &maps.w, kb * 64, (ut + i) * 64, full_bar(st));
+                        } else {
+                            const int ns = min(kps, nkb - kb);  // k-slices in this stage
+                            ttk::mbar_arrive_expect_tx(full_bar(st), (uint32_t)ns * (a_bytes + (uint32_t)nbox * kBBox));
+                            for (int s2 = 0; s2 < ns; ++s2) {
+                                const uint32_t sA = sbase + st * stage_bytes + (uint32_t)s2 * slice_bytes;
+                                const uint32_t sB = sA + a_bytes;
+                                ttk::tma_load_2d(sA, &maps.a, (kb + s2) * 64, mt * 128, full_bar(st));
+                                for (int i = 0; i < nbox; ++i)
+                                    ttk::tma_load_2d(sB + (uint32_t)i * kBBox, &maps.w, (kb + s2) * 64, (ut + i) * 64,
+                                                     full_bar(st));
+                            }
+                        }
                         if (++st == n_stages) {
                             st = 0;
                             ph ^= 1u;
@@ -256,18 +276,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     ttk::tc_fence_after();
-                    for (int kb = 0; kb < nkb; ++kb) {
+                    for (int kb = 0; kb < nkb; kb += kps) {
                         if (!ttk::mbar_wait(full_bar(st), ph)) {
                             ok = false;
                             break;
                         }
                         ttk::tc_fence_after();
-                        const uint32_t sA = sbase + st * stage_bytes, sB = sA + a_bytes;
+                        if (kps == 1) {  // the issue loop of wide tiles stays as short as it can be
+                            const uint32_t sA = sbase + st * stage_bytes, sB = sA + a_bytes;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ttk::mma_bf16_ss(tmem + a * 256u, ttk::sdesc_sw128(sA + 32u * k, 16, 1024),
-                                             ttk::sdesc_sw128(sB + 32u * k, 16, 1024), idesc,
-                                             (kb > 0 || k > 0) ? 1u : 0u);
+                            for (int k = 0; k < 4; ++k)
+                                ttk::mma_bf16_ss(tmem + a * 256u, ttk::sdesc_sw128(sA + 32u * k, 16, 1024),
+                                                 ttk::sdesc_sw128(sB + 32u * k, 16, 1024), idesc,
+                                                 (kb > 0 || k > 0) ? 1u : 0u);
+                        } else {
+                            const int ns = min(kps, nkb - kb);
+                            for (int s2 = 0; s2 < ns; ++s2) {
+                                const uint32_t sA = sbase + st * stage_bytes + (uint32_t)s2 * slice_bytes;
+                                const uint32_t sB = sA + a_bytes;
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    ttk::mma_bf16_ss(tmem + a * 256u, ttk::sdesc_sw128(sA + 32u * k, 16, 1024),
+                                                     ttk::sdesc_sw128(sB + 32u * k, 16, 1024), idesc,
+                                                     (kb + s2 > 0 || k > 0) ? 1u : 0u);
+                            }
+                        }
                         ttk::mma_commit(empty_bar(st));  // this stage is no longer read
                         if (++st == n_stages) {
                             st = 0;
