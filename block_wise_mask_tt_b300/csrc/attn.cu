@@ -100,6 +100,136 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Combine inside the split pass (fused): every non-empty split CTA of a row group
+// stores its partial state with plain stores, counts itself in on the group's ticket
+// (release), waits until all nv splits have (acquire, bounded), and then merges its
+// share of the group's rows, one softmax warp per row with every split's state in
+// flight.  The launch is cooperative (all CTAs resident), so no CTA waits for one that
+// cannot start.  The last CTA to finish resets the group's two counters.
+template <int D>
+__device__ __forceinline__ void fused_combine(const AttnSplitParams& p, uint32_t tO, int half, bool row_valid, int r_glob,
+                                           int b, int gkv, int rg, int split, int nv, int n_mt, bool ok, float m_run,
+                                           float l, int q, int lane_row, int tid, volatile int* s_go) {
+    constexpr int PER = D / 32;
+    const AttnGeom& g = p.g;
+    const int n_thr = 256 * n_mt;  // the softmax threads of this CTA
+    ttk::tc_fence_after();
+    const size_t pi = ((size_t)(b * g.Hkv + gkv) * g.n_splits + split) * (size_t)g.R + r_glob;
+#pragma unroll
+    for (int cc = 0; cc < D / 2; cc += 32) {
+        uint32_t o[32];
+        ttk::tmem_ld32(tO + half * (D / 2) + cc, o);  // warp-collective: every lane loads
+        ttk::tmem_ld_wait32(o);
+        if (row_valid) {
+            float4* dst = reinterpret_cast<float4*>(p.part_acc + pi * D + half * (D / 2) + cc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                __stcg(dst + e, make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                            __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3])));
+        }
+    }
+    if (row_valid && half == 0) {
+        p.part_ml[2 * pi + 0] = ok ? m_run : -CUDART_INF_F;
+        p.part_ml[2 * pi + 1] = ok ? l : 0.f;
+    }
+    __threadfence();
+    named_sync(4, n_thr);  // this CTA's partial state is written
+    const int rgi = (b * g.Hkv + gkv) * g.n_rg + rg;
+    unsigned* arrive = p.ticket + rgi;
+    unsigned* done = p.ticket + g.B * g.Hkv * g.n_rg + rgi;
+    if (q == 0 && lane_row == 0) {
+        unsigned v;
+        asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(v) : "l"(arrive) : "memory");
+        int go = 1;
+        const uint64_t t0 = ttk::globaltimer();
+        while (true) {
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(arrive) : "memory");
+            if (v >= (unsigned)nv) break;
+            if (ttk::globaltimer() - t0 > ttk::kWaitLimitNs) {
+                go = 0;
+                ttk::report_error(p.err, ttk::kErrTimeout);
+                break;
+            }
+            __nanosleep(64);
+        }
+        *s_go = go;
+    }
+    named_sync(4, n_thr);
+    if (*s_go != 0) {
+        // the group's rows, split evenly over its nv CTAs; a warp per row
+        const int lane = tid & 31;
+        const int w = (tid >> 5) - 4, n_w = n_thr / 32;
+        const int rg0 = rg * g.rows_per_cta;
+        const int rows = min(g.rows_per_cta, g.R - rg0);
+        const int r0 = (int)((long long)split * rows / nv), r1 = (int)((long long)(split + 1) * rows / nv);
+        const size_t base = (size_t)(b * g.Hkv + gkv) * g.n_splits * (size_t)g.R;
+        for (int r = r0 + w; r < r1; r += n_w) {
+            const int row = rg0 + r;
+            float m = -CUDART_INF_F, lsum = 0.f, acc[PER];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+            for (int c0 = 0; c0 < nv; c0 += 8) {
+                const int nc = min(8, nv - c0);
+                float mc[8], lc[8], a[8][PER];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const size_t pc = base + (size_t)(c0 + min(u, nc - 1)) * g.R + row;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pc);
+                    mc[u] = ml.x;
+                    lc[u] = ml.y;
+                    const float* ap = p.part_acc + pc * D + lane * PER;
+                    if (PER == 4) {
+                        const float4 v4 = __ldcg(reinterpret_cast<const float4*>(ap));
+                        a[u][0] = v4.x; a[u][1 % PER] = v4.y; a[u][2 % PER] = v4.z; a[u][3 % PER] = v4.w;
+                    } else {
+                        const float2 v2 = __ldcg(reinterpret_cast<const float2*>(ap));
+                        a[u][0] = v2.x; a[u][1 % PER] = v2.y;
+                    }
+                }
+                float mn = m;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (u < nc) mn = fmaxf(mn, mc[u]);
+                if (mn == -CUDART_INF_F) continue;
+                if (m != -CUDART_INF_F && mn != m) {
+                    const float rsc = exp2f(m - mn);
+                    lsum *= rsc;
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[e] *= rsc;
+                }
+                m = mn;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (u >= nc || mc[u] == -CUDART_INF_F) continue;
+                    const float wu = exp2f(mc[u] - m);
+                    lsum = fmaf(wu, lc[u], lsum);
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[e] = fmaf(wu, a[u][e], acc[e]);
+                }
+            }
+            const float inv = 1.0f / lsum;
+            const int s = row / g.G, j = row % g.G;
+            const size_t orow = ((size_t)b * g.S + s) * g.Hq + (size_t)gkv * g.G + j;
+            uint16_t* op = p.out + orow * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; e += 2) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+                *reinterpret_cast<uint32_t*>(op + e) = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            if (p.lse != nullptr && lane == 0) p.lse[orow] = (m + log2f(lsum)) * kLn2;
+        }
+    }
+    named_sync(4, n_thr);  // this CTA's merge reads are done
+    if (q == 0 && lane_row == 0) {
+        // every CTA of the group is past its wait once all have counted in here
+        const unsigned old = atomicAdd(done, 1u);
+        if (old == (unsigned)nv - 1u) {
+            *arrive = 0u;
+            *done = 0u;
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_split_kernel(const __grid_constant__ AttnSplitParams p,
@@ -514,7 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The tensor-store epilogue is chosen the same way by every thread of the CTA,
         // and every thread of a tile goes through its named barrier whether or not its
         // waits ran out (a partial state that ran out is marked empty instead).
-        if (direct ? maps.out_tma != 0 : true) {
+        if (!direct && g.fused) {
+            fused_combine<D>(p, tO, half, row_valid, r_glob, b, gkv, rg, split, nv, n_mt, ok, m_run, l, q, lane_row,
+                             tid, reinterpret_cast<volatile int*>(smem + C::kSlot + 8));
+        } else if (direct ? maps.out_tma != 0 : true) {
             // Epilogue: this half's D/2 columns of the O row go TMEM -> registers ->
             // 128-row x 128-byte boxes in shared memory (128-byte swizzle, so a warp's
             // stores of 32 rows fall in different banks; the Q tiles and the K/V ring
@@ -983,28 +1116,33 @@ bool attn_geometry(int B, int S, int Hq, int Hkv, int D, int max_ctx, int page_s
     g.lpt = (page_size != 0 && (long long)B * Hkv * g.n_rg * g.n_splits > 148 && tps + 1 <= kOrderMaxLen &&
              (long long)B * Hkv * g.n_rg * g.n_splits <= kOrderMaxUnits) ? 1 : 0;
     g.lpt_dyn = (g.lpt && dyn) ? 1 : 0;
+    g.fused = 0;  // the caller decides (it needs the device's SM count)
     return true;
 }
 
 // Workspace: fp32 partial accumulators [B][Hkv][n_splits][R][D], then (m, l) pairs,
-// then (ragged batches) the work order: units + 3 words.  Nothing in it carries over
-// from one call to the next.
-void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, int32_t** order) {
+// then two counters per row group (the combine inside the split pass; zero on entry,
+// left at zero), then (ragged batches) the work order: units + 3 words.
+void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml, unsigned** ticket,
+                 int32_t** order) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
+    size_t tk = (2 * (size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
     char* w = static_cast<char*>(ws);
     *part_acc = reinterpret_cast<float*>(w);
     *part_ml = reinterpret_cast<float*>(w + acc);
-    *order = g.lpt ? reinterpret_cast<int32_t*>(w + acc + ml) : nullptr;
+    *ticket = reinterpret_cast<unsigned*>(w + acc + ml);
+    *order = g.lpt ? reinterpret_cast<int32_t*>(w + acc + ml + tk) : nullptr;
 }
 
 size_t attn_workspace_bytes(const AttnGeom& g) {
     const size_t rows = (size_t)g.B * g.Hkv * g.n_splits * g.R;
     size_t acc = (rows * g.D * sizeof(float) + 255) & ~size_t(255);
     size_t ml = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
+    size_t tk = (2 * (size_t)g.B * g.Hkv * g.n_rg * sizeof(unsigned) + 255) & ~size_t(255);
     const size_t units = (size_t)g.B * g.Hkv * g.n_rg * g.n_splits;
-    return acc + ml + (g.lpt ? (units + 3) * sizeof(int32_t) : 0) + 256;
+    return acc + ml + tk + (g.lpt ? (units + 3) * sizeof(int32_t) : 0) + 256;
 }
 
 cudaError_t attn_split_prepare(int D) {
@@ -1032,6 +1170,24 @@ cudaError_t launch_attn_split(const AttnSplitParams& p, const AttnMaps& maps, cu
     const AttnGeom& g = p.g;
     const unsigned n_items = (unsigned)(g.B * g.Hkv * g.n_rg);
     dim3 grid = p.order ? dim3(n_items * (unsigned)g.n_splits, 1, 1) : dim3(n_items, (unsigned)g.n_splits, 1);
+    if (g.fused) {
+        // the CTAs of a row group wait for one another: a cooperative launch keeps
+        // every CTA resident (the caller checked that the grid fits one wave)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = g.D == 128 ? Cfg<128>::kBytes : Cfg<64>::kBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return g.D == 128 ? cudaLaunchKernelEx(&cfg, attn_split_kernel<128>, p, maps)
+                          : cudaLaunchKernelEx(&cfg, attn_split_kernel<64>, p, maps);
+    }
     if (g.D == 128)
         return launch_pdl(attn_split_kernel<128>, grid, dim3(kThreads), Cfg<128>::kBytes, stream, p, maps);
     else

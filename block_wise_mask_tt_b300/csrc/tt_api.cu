@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -204,6 +205,8 @@ tt_status plan_attn(const tt_attn_dims* d, const void* q, const void* k_blk, con
     return TT_OK;
 }
 
+tt_status sm_count(int* out);
+
 tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk, const void* v_blk,
                            const int32_t* page_table, const int32_t* ctx_len,
                            const int32_t* skip_if_zero, void* out, float* lse, void* ws,
@@ -217,9 +220,20 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     }
     float* part_acc = nullptr;
     float* part_ml = nullptr;
+    unsigned* ticket = nullptr;
     int32_t* order = nullptr;
     if (!pl.has_ctx) g.lpt = 0;
-    tti::attn_layout(g, ws, &part_acc, &part_ml, &order);
+    // Opt-in (TT_ATTN_FUSED_COMBINE=1 in the environment, read per call): split row
+    // groups of a contiguous cache whose whole grid fits one wave (one CTA per SM) are
+    // merged inside the split pass, without a combine launch.  Off by default: on the
+    // single-sequence and batched workloads the separate combine pass is faster.
+    int n_sms = 0;
+    TT_TRY(sm_count(&n_sms));
+    const char* fz = getenv("TT_ATTN_FUSED_COMBINE");
+    const bool fused_on = fz != nullptr && fz[0] == '1' && fz[1] == '\0';
+    g.fused = (fused_on && pl.has_ctx && g.page_size == 0 && g.n_splits > 1 && !g.lpt &&
+               (long long)g.B * g.Hkv * g.n_rg * g.n_splits <= n_sms) ? 1 : 0;
+    tti::attn_layout(g, ws, &part_acc, &part_ml, &ticket, &order);
     // Epilogue store maps: partial states when the context is split and a second pass
     // combines them; the output itself wherever a CTA may write it directly (when G
     // divides 128, so that a 128-row tile covers whole positions).
@@ -250,13 +264,14 @@ tt_status launch_attention(const AttnPlan& pl, const void* q, const void* k_blk,
     sp.skip_if_zero = skip_if_zero;
     sp.part_acc = part_acc;
     sp.part_ml = part_ml;
+    sp.ticket = ticket;
     sp.order = order;
     sp.out = static_cast<uint16_t*>(out);
     sp.lse = lse;
     sp.err = err;
     if (order != nullptr) TT_CUDA(tti::launch_attn_order(sp, st));
     TT_CUDA(tti::launch_attn_split(sp, maps, st));
-    if (g.n_splits > 1) {
+    if (g.n_splits > 1 && !g.fused) {
         tti::AttnMergeParams mp;
         mp.g = g;
         mp.order = order;

@@ -159,6 +159,8 @@ struct AttnGeom {
     int lpt;              // 1: work units dispatched longest first (ragged paged batches)
     int lpt_dyn;          // lpt: the prep kernel picks the split length per call from the
                           // active sequences (tiles_per_split times 1, 2, 4, ...)
+    int fused;            // split row groups are merged inside the split pass (its CTAs
+                          // all resident: a cooperative launch), no combine pass
     float scale_log2;     // softmax_scale * log2(e)
 };
 constexpr int kOrderMaxLen = 1024;       // longest unit (tiles) the longest-first order sorts
@@ -171,7 +173,7 @@ size_t attn_workspace_bytes(const AttnGeom& g);
 // the work units sorted by length, then their count, the split length of the call and
 // a flag that is 1 when some row group was split.
 void attn_layout(const AttnGeom& g, void* ws, float** part_acc, float** part_ml,
-                 int32_t** order);
+                 unsigned** ticket, int32_t** order);
 
 struct AttnSplitParams {
     AttnGeom g;
@@ -181,6 +183,8 @@ struct AttnSplitParams {
     const int32_t* skip_if_zero; // nullable
     float* part_acc;             // [B][Hkv][n_splits][R][D]
     float* part_ml;              // [B][Hkv][n_splits][R][2]
+    unsigned* ticket;            // fused: [2][B][Hkv][n_rg] arrivals, then finished merges;
+                                 // zero on entry and left at zero
     const int32_t* order;        // lpt: [units] work unit of each CTA, then the count
     uint16_t* out;               // bf16 [B][S][Hq][D]: written here by the CTAs of row
                                  // groups with one non-empty split

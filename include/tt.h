@@ -124,10 +124,15 @@ TT_API tt_status tt_adaln_modulate(const void* x, const float* shift, const floa
  *   out          bf16 [B][S][Hq][D]                (out)
  *   lse          fp32 [B][S][Hq] natural-log sum-exp, or NULL              (out)
  *   workspace    device scratch of tt_denoise_attn_workspace(dims) bytes for the
- *                per-split partial softmax states and, on ragged paged batches, the
- *                order in which the work units run.  No state carries from one call
- *                to the next, so its contents on entry do not matter.  Calls that
- *                share a workspace must not overlap on the device.
+ *                per-split partial softmax states, two counters per row group (used
+ *                when TT_ATTN_FUSED_COMBINE=1 is set in the environment: split CTAs
+ *                then merge their row groups themselves; read when a call is
+ *                enqueued, so a captured block graph keeps the mode it was captured
+ *                with) and, on ragged paged
+ *                batches, the order in which the work units run.  Must be
+ *                zero-filled before its first use; every call leaves the counters at
+ *                zero again.  Calls that share a workspace must not overlap on the
+ *                device.
  * A page id outside [0, num_pages) or a ctx_len outside range skips that sequence's
  * context and sets TT_ERR_DEVICE.
  * -------------------------------------------------------------------------------- */

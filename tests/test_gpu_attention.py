@@ -132,6 +132,34 @@ def test_small_ragged_batch_in_128_row_groups(tt):
     check_attention(O, Or, lse, lr, what="128-row groups")
 
 
+@pytest.mark.parametrize("splits", [2, 5, 16])
+def test_fused_combine_option(tt, splits, monkeypatch):
+    """With TT_ATTN_FUSED_COMBINE=1 the split CTAs of a contiguous call that fits one
+    wave merge their row groups themselves (counters in the workspace, left at zero):
+    three calls on one workspace, a ragged batch with some sequences shorter than one
+    split, each against the oracle."""
+    monkeypatch.setenv("TT_ATTN_FUSED_COMBINE", "1")
+    w = W(B=3, L=2600, L_min=100, S=16, Hq=32, Hkv=2, D=128, q_prescale=1 / math.sqrt(128))
+    inp = synth.make_attention_inputs(w, seed=18)
+    L = inp["k_ctx"].shape[1]
+    dims = tt.attn_dims(w.B, w.S, w.Hq, w.Hkv, w.D, L, 0, 0, 0, w.softmax_scale, splits)
+    ws = tt.workspace(tt.tt_denoise_attn_workspace(dims))
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    args = [dev(inp[k]) for k in ("q", "k_blk", "v_blk", "k_ctx", "v_ctx")]
+    cl = dev(inp["ctx_len"])
+    for call in range(3):
+        g_out, out = guarded(w.B * w.S * w.Hq * w.D, torch.int16, 0x7FC0)
+        g_lse, lse = guarded(w.B * w.S * w.Hq, torch.float32, float("nan"))
+        tt.tt_denoise_attn(dims, *args, None, cl, out, lse, ws=ws)
+        torch.cuda.synchronize()
+        assert tt.tt_device_status(True) == 0
+        check_guards(g_out, 0x7FC0, "out")
+        check_guards(g_lse, float("nan"), "lse")
+        O = bf16_to_f64(host(out)).reshape(w.B, w.S, w.Hq, w.D)
+        check_attention(O, Or, host(lse).astype(np.float64).reshape(w.B, w.S, w.Hq), lr,
+                        what=f"fused combine, {splits} splits, call {call}")
+
+
 def test_paged_equals_contiguous(tt):
     w = W(B=3, L=500, L_min=1, S=16, Hq=32, Hkv=2, D=128, paged=True, q_prescale=1 / math.sqrt(128))
     inp = synth.make_attention_inputs(w, seed=12)
