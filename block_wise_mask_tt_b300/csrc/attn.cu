@@ -886,11 +886,13 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
 // Output: order[0 .. count) units, order[n_units] = count, order[n_units + 1] = split
 // length, order[n_units + 2] = 1 if some row group has more than one split.
 constexpr int kOrderThreads = 1024;
-constexpr int kOrderCands = 8;  // split lengths tried: tiles_per_split << 0 .. 7
+constexpr int kOrderCands = 8;     // split lengths tried: tiles_per_split << 0 .. 7
+constexpr int kOrderCache = 4096;  // items whose tile counts stay in shared memory
 __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_constant__ AttnSplitParams p) {
     ttk::pdl_wait();
     ttk::pdl_trigger();
     __shared__ int hist[kOrderMaxLen + 1];
+    __shared__ int s_tiles[kOrderCache];
     __shared__ unsigned s_total, s_lmax, s_active, s_units[kOrderCands];
     __shared__ int s_tps, s_split;
     const AttnGeom& g = p.g;
@@ -898,12 +900,15 @@ __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_
     const int n_units = n_items * g.n_splits;
     const int cap = g.page_size ? g.max_pages * g.page_size : g.max_ctx;
     const int base = g.tiles_per_split;
+    const bool cached = n_items <= kOrderCache;
+    const int lane = threadIdx.x & 31;
     int32_t* order = const_cast<int32_t*>(p.order);
     // context tiles of an item's sequence, or -1 when it takes no part in this call
     auto item_tiles = [&](int item) -> int {
         const int b = item / (g.n_rg * g.Hkv);
-        if (p.skip_if_zero != nullptr && __ldg(p.skip_if_zero + b) == 0) return -1;
+        const int keep = p.skip_if_zero != nullptr ? __ldg(p.skip_if_zero + b) : 1;
         const int ctx = p.ctx_len ? __ldg(p.ctx_len + b) : g.max_ctx;
+        if (keep == 0) return -1;
         if (ctx < 0 || ctx > cap) return 0;  // split 0 alone: the split pass reports it
         return (ctx + kTileKeys - 1) / kTileKeys;
     };
@@ -915,25 +920,27 @@ __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_
         for (int c = 0; c < kOrderCands; ++c) s_units[c] = 0;
     }
     __syncthreads();
-    if (g.lpt_dyn) {
-        // Sums over the items (each below 2^31: at most kOrderMaxUnits items of at most
-        // kOrderMaxLen tiles), reduced per warp, one shared atomic per warp and sum.
-        unsigned tot = 0, lmax = 0, active = 0, units[kOrderCands] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int it = threadIdx.x; it < n_items; it += kOrderThreads) {
-            const int L = item_tiles(it);
-            if (L < 0) continue;
-            ++active;
-            tot += (unsigned)L + 1u;
-            lmax = max(lmax, (unsigned)L);
+    // Sums over the items (each below 2^31: at most kOrderMaxUnits items of at most
+    // kOrderMaxLen tiles), reduced per warp, one shared atomic per warp and sum; the
+    // tile counts are kept for the two passes over the units.
+    unsigned tot = 0, lmax = 0, active = 0, units[kOrderCands] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int it = threadIdx.x; it < ((cached || g.lpt_dyn) ? n_items : 0); it += kOrderThreads) {
+        const int L = item_tiles(it);
+        if (cached) s_tiles[it] = L;
+        if (L < 0 || !g.lpt_dyn) continue;
+        ++active;
+        tot += (unsigned)L + 1u;
+        lmax = max(lmax, (unsigned)L);
 #pragma unroll
-            for (int c = 0; c < kOrderCands; ++c) units[c] += (unsigned)max(1, (L + (base << c) - 1) / (base << c));
-        }
+        for (int c = 0; c < kOrderCands; ++c) units[c] += (unsigned)max(1, (L + (base << c) - 1) / (base << c));
+    }
+    if (g.lpt_dyn) {
         tot = __reduce_add_sync(0xffffffffu, tot);
         lmax = __reduce_max_sync(0xffffffffu, lmax);
         active = __reduce_add_sync(0xffffffffu, active);
 #pragma unroll
         for (int c = 0; c < kOrderCands; ++c) units[c] = __reduce_add_sync(0xffffffffu, units[c]);
-        if ((threadIdx.x & 31) == 0) {
+        if (lane == 0 && active != 0) {
             atomicAdd(&s_total, tot);
             atomicMax(&s_lmax, lmax);
             atomicAdd(&s_active, active);
@@ -967,17 +974,22 @@ __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_
     }
     __syncthreads();
     const int tps = s_tps;
-    auto unit_len = [&](int u) -> int {
+    // Length class of unit u (0: empty).  Units are walked in whole-warp steps and the
+    // lanes of one class share one shared-memory atomic: most units of a split batch
+    // have the same length, and one atomic per unit would queue on that counter.
+    auto unit_class = [&](int u) -> int {
+        if (u >= n_units) return 0;
         const int item = u % n_items, split = u / n_items;
-        const int L = item_tiles(item);
+        const int L = cached ? s_tiles[item] : item_tiles(item);
         if (L < 0) return 0;
         const int t0 = split * tps;
         const int t1 = min(L, t0 + tps);
-        return (split == 0 ? 1 : 0) + max(0, t1 - t0);
+        return min((split == 0 ? 1 : 0) + max(0, t1 - t0), kOrderMaxLen);
     };
-    for (int u = threadIdx.x; u < n_units; u += kOrderThreads) {
-        const int len = unit_len(u);
-        if (len > 0) atomicAdd(&hist[min(len, kOrderMaxLen)], 1);
+    for (int u0 = 0; u0 < n_units; u0 += kOrderThreads) {
+        const int cls = unit_class(u0 + (int)threadIdx.x);
+        const unsigned peers = __match_any_sync(0xffffffffu, cls);
+        if (cls > 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[cls], __popc(peers));
     }
     __syncthreads();
     {
@@ -986,7 +998,7 @@ __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_
         // totals)
         static_assert(kOrderThreads == kOrderMaxLen, "one length per thread");
         __shared__ int wsum[kOrderThreads / 32];
-        const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+        const int t = threadIdx.x, warp = t >> 5;
         const int len = kOrderMaxLen - t;
         const int c = hist[len];
         int incl = c;
@@ -1016,9 +1028,15 @@ __global__ void __launch_bounds__(kOrderThreads) attn_order_kernel(const __grid_
         }
     }
     __syncthreads();
-    for (int u = threadIdx.x; u < n_units; u += kOrderThreads) {
-        const int len = unit_len(u);
-        if (len > 0) order[atomicAdd(&hist[min(len, kOrderMaxLen)], 1)] = u;
+    for (int u0 = 0; u0 < n_units; u0 += kOrderThreads) {
+        const int u = u0 + (int)threadIdx.x;
+        const int cls = unit_class(u);
+        const unsigned peers = __match_any_sync(0xffffffffu, cls);
+        const int leader = __ffs(peers) - 1;
+        int slot = 0;
+        if (cls > 0 && lane == leader) slot = atomicAdd(&hist[cls], __popc(peers));
+        slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(peers & ((1u << lane) - 1u));
+        if (cls > 0) order[slot] = u;
     }
 }
 
