@@ -132,6 +132,17 @@ def test_small_ragged_batch_in_128_row_groups(tt):
     check_attention(O, Or, lse, lr, what="128-row groups")
 
 
+def test_ragged_batch_beyond_the_order_kernels_tile_cache(tt):
+    """More row-group items (4100 sequences x 1 kv head x 1 group) than the prep kernel
+    keeps tile counts for in shared memory (4096): its two passes over the units then
+    read ctx_len from global memory.  One-tile contexts of 1..128 tokens, S = 1."""
+    w = W(B=4100, L=128, L_min=1, S=1, Hq=1, Hkv=1, D=64, paged=True, softmax_scale=0.125)
+    inp = synth.make_attention_inputs(w, seed=23)
+    O, lse = run_attn(tt, w, inp)
+    Or, lr = oracle.denoise_attention(inp, w.softmax_scale)
+    check_attention(O, Or, lse, lr, what="4100 one-tile sequences")
+
+
 @pytest.mark.parametrize("splits", [2, 5, 16])
 def test_fused_combine_option(tt, splits, monkeypatch):
     """With TT_ATTN_FUSED_COMBINE=1 the split CTAs of a contiguous call that fits one
